@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark: INT4 block-quantized MoE FFN layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config decode|tiny|verify|prefill|stack]
+
+A step is one pass of the whole layer (router, expert FFNs, weighted
+combine) over one batch of T tokens.  The default workload is the
+Qwen1.5-MoE-A2.7B-shaped decode layer (T=1, H=2048, I=1408, E=60, top-4,
+uint4 block 32 with zero points, fp16).  Weights rotate over a pool of
+independent layers far larger than L2, so every step streams its experts
+from HBM.  Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle (the correctness reference) on
+the same workload instead: a deliberately slow baseline, not a target.
+N > 1 (torchrun): independent replicas, one per GPU, no collective on the
+data path; value = tokens of all ranks / the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "QMoE layer tokens/s; decode HBM GB/s and prefill TFLOPS as % of GB300 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24}
+DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 240}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode", choices=list(POOL))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS[a.config]
+    if a.warmup is None:
+        a.warmup = max(3, min(240, a.steps // 10))
+    a.warmup = max(3, a.warmup)
+    return a
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_init():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_bytes(wl, D):
+    """Algorithmic bytes: weights of the D distinct selected experts, router, x, out."""
+    from int4_block_quantized_gb300 import synthetic as S
+    A = wl.T * wl.k
+    nbh, nbi = wl.H // wl.block_size, wl.I // wl.block_size
+    zp = 1 if wl.has_zp else 0
+    gu = 2 * wl.I * (wl.H // 2 + nbh * 2 + nbh * zp)          # gate + up of one expert
+    dn = wl.H * (wl.I // 2 + nbi * 2 + nbi * zp)               # down of one expert
+    assert gu + dn == S.expert_bytes(wl)
+    router = wl.H * wl.E * 2 + (wl.E * 4 if wl.zipf_s else 0)
+    xio = 2 * wl.T * wl.H * 2
+    layer = D * (gu + dn) + router + xio
+    gateup_kernel = D * gu + wl.T * wl.H * 2 + A * wl.I * 4    # x in, fp32 act out
+    down_kernel = D * dn + A * wl.I * 4 + wl.T * wl.H * 2      # act in, out
+    flops = 2 * A * 3 * wl.H * wl.I + 2 * wl.T * wl.H * wl.E
+    return dict(layer=layer, gateup=gateup_kernel, down=down_kernel, flops=flops)
+
+
+def cpu_baseline(wl, layer_cpu, xs_cpu, budget_s=12.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of tokens."""
+    import oracle
+    t0 = time.perf_counter()
+    tokens = 0
+    i = 0
+    while True:
+        L = dict(layer_cpu, x=xs_cpu[i % len(xs_cpu)], T=xs_cpu[i % len(xs_cpu)].shape[0])
+        oracle.qmoe_forward(L)
+        tokens += L["T"]
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return tokens / el, tokens, el
+
+
+def run_reference(a, wl):
+    """--impl reference: the fp64 oracle on the host cores, same workload."""
+    import torch
+    from int4_block_quantized_gb300 import synthetic as S
+    import oracle
+    oracle._load()
+    layer = S.make_weights(wl, seed=0, device="cpu", layer=0)
+    T1 = min(wl.T, 1 if wl.T <= 16 else 4)  # one step = a bounded sample of the batch
+    xs = [S.make_x(wl, seed=0, device="cpu", T=T1, layer=l) for l in range(4)]
+    budget = 150.0
+    # warm-up steps (untimed), then timed steps within the budget
+    tw0 = time.perf_counter()
+    for i in range(a.warmup):
+        oracle.qmoe_forward(dict(layer, x=xs[i % 4], T=T1))
+        if time.perf_counter() - tw0 > 20.0:
+            break
+    t0 = time.perf_counter()
+    steps = 0
+    while steps < a.steps:
+        oracle.qmoe_forward(dict(layer, x=xs[steps % 4], T=T1))
+        steps += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    el = time.perf_counter() - t0
+    v = steps * T1 / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": a.gpus,
+        "steps": steps, "warmup": a.warmup, "ms_per_step": 1000.0 * el / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(wl, a),
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d step(s) of %d token(s) of the %s workload through one layer "
+                                   "(all %d experts resident), fp64, one thread" % (steps, T1, wl.name, wl.E)},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def config_dict(wl, a):
+    return {"workload": "%s: T=%d H=%d I=%d E=%d k=%d block=%d %s act, %s scales, %s" % (
+        wl.name, wl.T, wl.H, wl.I, wl.E, wl.k, wl.block_size, "bf16" if wl.act_dtype else "fp16",
+        "bf16" if wl.scale_dtype else "fp16", "uint4 zero points" if wl.has_zp else "no zero points"),
+        "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "block_size": wl.block_size,
+        "pool_layers": POOL[wl.name] if wl.name in POOL else 1,
+        "l2": "weights rotate over %d independent layers (> L2 per revisit); no flush" % POOL.get(wl.name, 1),
+        "parallelism": "replicas x%d" % a.gpus}
+
+
+def run_ours(a, wl):
+    import torch
+    from int4_block_quantized_gb300 import binding as B
+    from int4_block_quantized_gb300 import synthetic as S
+    rank, world, local = dist_init()
+    dev = torch.device("cuda", local)
+    B.lib()
+    P = POOL[wl.name]
+    layers = [S.make_weights(wl, seed=0, device=dev, layer=l) for l in range(P)]
+    xs = [S.make_x(wl, seed=0, device=dev, layer=l) for l in range(P)]
+    outs = [torch.empty_like(x) for x in xs]
+    ws = B.Workspace(wl.T, wl.H, wl.I, wl.E, wl.k, device=dev)
+    # distinct experts per pool layer (for the algorithmic byte count)
+    Ds = []
+    for l in range(P):
+        _, ti, _, _ = B.qmoe_route(xs[l], layers[l]["router_w"], wl.k, layers[l]["router_bias"], ws=ws)
+        Ds.append(int(torch.unique(ti).numel()))
+    D_mean = sum(Ds) / len(Ds)
+    wb = workload_bytes(wl, D_mean)
+
+    def step(i):
+        j = i % P
+        B.qmoe_forward(layers[j], x=xs[j], out=outs[j], ws=ws)
+
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for i in range(3):
+            step(i)
+    torch.cuda.synchronize(dev)
+    G = min(a.steps, 24 * P if wl.T <= 16 else 2 * P)
+
+    def capture(n, start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                step(start + i)
+        return g
+
+    g_warm = capture(a.warmup, 0)
+    g_main = capture(G, a.warmup)
+    rem = a.steps % G
+    g_rem = capture(rem, a.warmup) if rem else None
+    reps = a.steps // G
+    g_warm.replay()
+    torch.cuda.synchronize(dev)
+
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(s)
+    e1.synchronize()
+    ck = clocks.stop()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    value = wl.T * a.steps * world / (ms / 1000.0)
+
+    # ---- per-kernel durations (events between kernels, no overlap) for the roofline
+    nk = 3
+    dur = [[] for _ in range(nk)]
+    with torch.cuda.stream(s):
+        for rep in range(3):
+            for j in range(P):
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+                B.qmoe_forward_profiled(layers[j], evs, x=xs[j], out=outs[j], ws=ws)
+                if rep > 0:
+                    for kk in range(nk):
+                        dur[kk].append((evs, kk))
+    torch.cuda.synchronize(dev)
+    kms = [statistics.mean(evs[kk].elapsed_time(evs[kk + 1]) for evs, _ in dur[kk]) for kk in range(nk)]
+    pk = peaks()
+    gu_gbs = wb["gateup"] / (kms[1] * 1e-3) / 1e9
+
+    # ---- end to end through the public API: pinned H2D of x, forward, D2H of out
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = [torch.empty_like(x, device="cpu").pin_memory() for x in xs]
+    xd = torch.empty_like(xs[0])
+    od = torch.empty_like(xs[0])
+    n_e2e = min(a.steps, 4000)
+    with torch.cuda.stream(s):
+        for i in range(3):
+            xd.copy_(xh[i % P], non_blocking=True)
+            B.qmoe_forward(layers[i % P], x=xd, out=od, ws=ws)
+            oh[i % P].copy_(od, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(s)
+        for i in range(n_e2e):
+            j = i % P
+            xd.copy_(xh[j], non_blocking=True)
+            B.qmoe_forward(layers[j], x=xd, out=od, ws=ws)
+            oh[j].copy_(od, non_blocking=True)
+        f1.record(s)
+    f1.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
+    e2e_value = wl.T * n_e2e * world / (e2e_ms / 1000.0)
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        lc = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in layers[0].items()}
+        xc = [x.cpu() for x in xs[:4]]
+        v, toks, el = cpu_baseline(wl, lc, xc)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": "%d token(s) of the %s workload through one layer in %.1f s, fp64, one thread"
+                         % (toks, wl.name, el)}
+
+    if rank == 0:
+        ms_step = ms / a.steps
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16" if wl.act_dtype == 0 else "bf16",
+            "data": "synthetic", "config": config_dict(wl, a),
+            "roofline": {"bound": "hbm", "kernel": "decode gate-up (+SwiGLU)",
+                         "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gu_gbs / pk["hbm_gbs"], "traffic": None,
+                         "peak_source": pk["source"],
+                         "bytes_per_launch": wb["gateup"], "launch_ms": kms[1]},
+            "layer": {"bytes": wb["layer"], "distinct_experts": D_mean,
+                      "hbm_gbs": wb["layer"] / (ms_step * 1e-3) / 1e9,
+                      "hbm_frac": wb["layer"] / (ms_step * 1e-3) / 1e9 / pk["hbm_gbs"],
+                      "kernel_ms": {"route": kms[0], "gateup": kms[1], "down": kms[2]},
+                      "tflops": wb["flops"] / (ms_step * 1e-3) / 1e12},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,
+                    "steps": n_e2e},
+            "gpu_launches": 3 * a.steps,
+            "clocks": {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
+                       "samples": ck["samples"]},
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    a = parse()
+    from int4_block_quantized_gb300 import synthetic as S
+    wl = S.WORKLOADS[a.config]
+    if a.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if world > 1 and rank != 0:
+            return
+        run_reference(a, wl)
+        return
+    run_ours(a, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+/*
+ * qmoe.h -- C ABI of the INT4 block-quantized mixture-of-experts FFN layer
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (source: "Qwen MoE BringUp", IREE ONNX Runtime EP issue #34,
+ * the Qwen1.5-MoE-A2.7B-Chat INT4 IR Guide, section 3 "MoE Block"):
+ *   logits = x . router_w (+ router_bias)          (Router: gate linear)
+ *   p      = softmax(logits) over all E experts     (Router, kernel step 1)
+ *   top-k  = the k largest p, best first            (Router, kernel step 2)
+ *   for each chosen expert e of token t:
+ *     g = x . Wg_e^T, u = x . Wu_e^T                (Expert Computation, step 4)
+ *     act = g * sigmoid(g) * u                      (step 5, SwiGLU)
+ *     y = act . Wd_e^T                              (step 6)
+ *   out[t] = sum_j p[t, j] * y_j                    (step 7, not renormalised)
+ * with every expert weight dequantised per DequantizeLinear with block_size
+ * along the input dimension: w = (q - zp) * scale ("Qwen MoE BringUp",
+ * local fix A1: extui -> uitofp -> subf -> mulf).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every tensor pointer is a DEVICE pointer owned by the caller
+ *   (cudaMalloc, torch, ...), on the current CUDA device, contiguous
+ *   row-major.  The library never allocates, frees or copies host memory
+ *   and never synchronises; all work is enqueued on `stream` (a
+ *   cudaStream_t passed as void*, NULL = the legacy default stream).
+ * Packed weights.  A projection with N outputs and K inputs, for all E
+ *   experts, is three tensors:
+ *     w      uint8  [E, N, K/2]   two uint4 codes per byte; element k of a
+ *                                 row is in byte k/2, LOW nibble for even k
+ *     scales fp16 or bf16 [E, N, K/block_size]
+ *     zp     uint8  [E, N, K/block_size], values 0..15, or NULL meaning
+ *                                 zero point 8 (signed symmetric int4)
+ *   This is the IR guide's pre-transposed layout ([out, in], Optimization
+ *   Opportunities item 5); gate/up have N = I, K = H; down has N = H, K = I.
+ * Alignment.  x, out, router_w and every w must be 16-byte aligned; K must
+ *   be a multiple of 32 and of block_size; block_size is 32, 64 or 128.
+ * Errors.  Arguments are checked on the host before anything is enqueued;
+ *   a bad argument returns QMOE_ERR_INVALID_ARG / QMOE_ERR_UNSUPPORTED /
+ *   QMOE_ERR_WORKSPACE and enqueues nothing.  A failed launch returns
+ *   QMOE_ERR_CUDA.  Conditions found on the device (a bounded wait that ran
+ *   out) set bits in a status word kept in the workspace; read and clear it
+ *   with qmoe_get_device_status.  No C++ exception crosses this ABI.
+ * Device.  Compute capability 10.3 (sm_103a) only; any other device
+ *   returns QMOE_ERR_UNSUPPORTED.  There is no CPU fallback.
+ * Concurrency.  Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef QMOE_H_
+#define QMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QMOE_OK = 0,
+  QMOE_ERR_INVALID_ARG = 1,  /* NULL / out-of-range / misaligned argument   */
+  QMOE_ERR_UNSUPPORTED = 2,  /* valid but not supported (device, shape)     */
+  QMOE_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required     */
+  QMOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed        */
+  QMOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait ran out       */
+  QMOE_ERR_DEVICE_CHECK = 6  /* device status: an index check failed        */
+} qmoe_status;
+
+typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
+
+/* Path selection for qmoe_forward_ex (tests force one path to compare both). */
+typedef enum { QMOE_PATH_AUTO = 0, QMOE_PATH_DECODE = 1, QMOE_PATH_PREFILL = 2 } qmoe_path;
+
+/* One projection for all E experts (see "Packed weights" above). */
+typedef struct {
+  const uint8_t* w;
+  const void* scales;
+  const uint8_t* zp; /* may be NULL: zero point 8 */
+} qmoe_qweight;
+
+/* Largest shapes accepted: E <= 256 experts, 1 <= k <= 8. */
+#define QMOE_MAX_EXPERTS 256
+#define QMOE_MAX_TOPK 8
+/* Tokens at or below this count take the decode (GEMV) path under QMOE_PATH_AUTO. */
+#define QMOE_DECODE_MAX_TOKENS 16
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* qmoe_status_string(int status);
+
+/* Bytes of device workspace qmoe_route / qmoe_forward need for these
+ * shapes (covers both paths).  The workspace is caller-owned, 256-byte
+ * aligned device memory.  Before its FIRST use it must be prepared with
+ * qmoe_workspace_init; every call leaves it ready for the next one. */
+size_t qmoe_workspace_size(int T, int H, int I, int E, int k);
+
+/* Zero the workspace's control words (counters, device status) on `stream`. */
+int qmoe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Router: logits = x[T,H] . router_w[H,E] (+ router_bias[E]) accumulated in
+ * fp32; softmax over all E in fp32; the k largest probabilities, best first,
+ * equal probabilities ordered by lower expert id; weights are the raw
+ * probabilities (not renormalised).  Then the assignments a = t*k + j are
+ * grouped by expert ("sort tokens by expert", IR guide Optimization
+ * Opportunities item 9 step 1).
+ *   x, router_w : act_dtype (fp16 or bf16), [T,H] and [H,E]
+ *   router_bias : fp32 [E] or NULL
+ *   topk_w      : fp32 [T,k] out;  topk_ids : int32 [T,k] out
+ *   expert_offsets : int32 [E+1] out or NULL: offsets[e] = number of
+ *                 assignments to experts < e, offsets[E] = T*k
+ *   perm        : int32 [T*k] out or NULL: assignment ids grouped by
+ *                 expert, increasing within an expert
+ * Requires 1 <= T, 1 <= k <= min(E, 8), E <= 256. */
+int qmoe_route(const void* x, const void* router_w, int act_dtype, const float* router_bias,
+               int T, int H, int E, int k, float* topk_w, int32_t* topk_ids,
+               int32_t* expert_offsets, int32_t* perm, void* workspace, size_t workspace_bytes,
+               void* stream);
+
+/* MatMulNBits: y[M,N] = x[M,K] . dequant(W)[N,K]^T with W one packed
+ * [N, K/2] matrix (E = 1 in the layout above), fp32 accumulation, y rounded
+ * to act_dtype.  Small M streams W through CUDA cores; no workspace. */
+int matmul_nbits(const void* x, int act_dtype, const uint8_t* w, const void* scales,
+                 int scale_dtype, const uint8_t* zp, int M, int N, int K, int block_size, void* y,
+                 void* stream);
+
+/* The whole layer: out[T,H] (act_dtype) = sum over the k chosen experts of
+ * p * SwiGLU-FFN_e(x).  gate/up are [E, I, H/2] (N = I, K = H), down is
+ * [E, H, I/2] (N = H, K = I); all three share scale_dtype and block_size.
+ * topk_w_out / topk_ids_out ([T,k], may be NULL) return the routing used.
+ * If accumulate is non-zero, out = out + layer(x) (residual add).
+ * Requires H and I multiples of 32 and of block_size. */
+int qmoe_forward(const void* x, int act_dtype, const void* router_w, const float* router_bias,
+                 qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
+                 int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
+                 int32_t* topk_ids_out, int accumulate, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* qmoe_forward with an explicit path (QMOE_PATH_*); AUTO picks decode for
+ * T <= QMOE_DECODE_MAX_TOKENS. */
+int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const float* router_bias,
+                    qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
+                    int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
+                    int32_t* topk_ids_out, int accumulate, int path, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* qmoe_forward_ex for profiling: records events[0] before the first kernel
+ * and events[i] after kernel i (router, gate-up, down on the decode path),
+ * for i < n_events (cudaEvent_t passed as void*; NULL entries skipped).  The
+ * kernels run back to back without programmatic overlap, so event pairs
+ * bracket one kernel each.  Same arguments and results as qmoe_forward. */
+int qmoe_forward_profiled(const void* x, int act_dtype, const void* router_w,
+                          const float* router_bias, qmoe_qweight gate, qmoe_qweight up,
+                          qmoe_qweight down, int scale_dtype, int T, int H, int I, int E, int k,
+                          int block_size, void* out, int path, void* workspace,
+                          size_t workspace_bytes, void* stream, void* const* events,
+                          int n_events);
+
+/* DequantizeLinear of one [N, K] matrix (packed [N, K/2]) to fp32 out[N,K]:
+ * (q - zp) * scale, which fp32 holds exactly. */
+int qmoe_dequant(const uint8_t* w, const void* scales, int scale_dtype, const uint8_t* zp, int N,
+                 int K, int block_size, float* out, void* stream);
+
+/* RMSNorm of the layer stack ("IR guide", 1. RMSNorm) with unit weight:
+ * out[t,h] = x[t,h] / sqrt(mean_h(x[t,h]^2) + eps), computed in fp32 and
+ * rounded to act_dtype.  x and out may alias. */
+int qmoe_rmsnorm(const void* x, void* out, int act_dtype, int T, int H, float eps, void* stream);
+
+/* Read (blocking: synchronises `stream`) and clear the device status word
+ * of `workspace`.  Returns QMOE_OK, or the first QMOE_ERR_* recorded by a
+ * kernel since the last read; *bits_out (may be NULL) gets the raw bits. */
+int qmoe_get_device_status(void* workspace, uint32_t* bits_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMOE_H_ */

@@ -1,0 +1,201 @@
+"""Thin Python binding of the C ABI (include/qmoe.h) over ctypes.
+
+Argument marshalling only: every step of the layer runs in the CUDA library
+libqmoe.so.  Tensors are torch CUDA tensors (device memory and streams come
+from PyTorch); calls are enqueued on torch's current stream.  There is no
+fallback: if the library is missing this module raises on import use.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmoe.so")
+
+F16, BF16 = 0, 1
+PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+DECODE_MAX_TOKENS = 16
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported device or shape",
+           3: "workspace missing or too small", 4: "CUDA runtime error",
+           5: "device wait timed out", 6: "device index check failed"}
+
+
+class QMoEError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s: %s (status %d)" % (where, _STATUS.get(code, "unknown"), code))
+
+
+class QWeight(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zp", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libqmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libqmoe.so not built (run int4_block_quantized_gb300/build.py); "
+                               "there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.qmoe_status_string.restype = ctypes.c_char_p
+        L.qmoe_status_string.argtypes = [i32]
+        L.qmoe_workspace_size.restype = sz
+        L.qmoe_workspace_size.argtypes = [i32] * 5
+        L.qmoe_workspace_init.restype = i32
+        L.qmoe_workspace_init.argtypes = [vp, sz, vp]
+        L.qmoe_route.restype = i32
+        L.qmoe_route.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+        L.matmul_nbits.restype = i32
+        L.matmul_nbits.argtypes = [vp, i32, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]
+        L.qmoe_forward.restype = i32
+        L.qmoe_forward.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
+            [vp, vp, vp, i32, vp, sz, vp]
+        L.qmoe_forward_ex.restype = i32
+        L.qmoe_forward_ex.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
+            [vp, vp, vp, i32, i32, vp, sz, vp]
+        L.qmoe_forward_profiled.restype = i32
+        L.qmoe_forward_profiled.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
+            [vp, i32, vp, sz, vp, ctypes.POINTER(ctypes.c_void_p), i32]
+        L.qmoe_dequant.restype = i32
+        L.qmoe_dequant.argtypes = [vp, vp, i32, vp, i32, i32, i32, vp, vp]
+        L.qmoe_rmsnorm.restype = i32
+        L.qmoe_rmsnorm.argtypes = [vp, vp, i32, i32, i32, ctypes.c_float, vp]
+        L.qmoe_get_device_status.restype = i32
+        L.qmoe_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(t):
+    return BF16 if t.dtype == torch.bfloat16 else F16
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise QMoEError(rc, where)
+
+
+def qmoe_status_string(code):
+    return lib().qmoe_status_string(code).decode()
+
+
+def qmoe_workspace_size(T, H, I, E, k):
+    return int(lib().qmoe_workspace_size(T, H, I, E, k))
+
+
+class Workspace:
+    """Caller-owned device workspace sized for (T, H, I, E, k), initialised once."""
+
+    def __init__(self, T, H, I, E, k, device=None):
+        self.nbytes = qmoe_workspace_size(T, H, I, E, k)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        _check(lib().qmoe_workspace_init(_p(self.buf), self.nbytes, _stream()), "qmoe_workspace_init")
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    def status(self):
+        bits = ctypes.c_uint32(0)
+        rc = lib().qmoe_get_device_status(self.ptr, ctypes.byref(bits), _stream())
+        return rc, bits.value
+
+
+def qmoe_route(x, router_w, k, router_bias=None, ws=None, grouping=True):
+    """(topk_w [T,k] fp32, topk_ids [T,k] int32, offsets [E+1], perm [T*k])."""
+    T, H = x.shape
+    E = router_w.shape[1]
+    ws = ws or Workspace(T, H, 32, E, k, device=x.device)
+    tw = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    ti = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    off = torch.empty(E + 1, dtype=torch.int32, device=x.device) if grouping else None
+    perm = torch.empty(T * k, dtype=torch.int32, device=x.device) if grouping else None
+    _check(lib().qmoe_route(_p(x), _p(router_w), _dt(x), _p(router_bias), T, H, E, k, _p(tw), _p(ti),
+                            _p(off), _p(perm), ws.ptr, ws.nbytes, _stream()), "qmoe_route")
+    return tw, ti, off, perm
+
+
+def matmul_nbits(x, w, scales, zp, block_size, out=None):
+    """y[M,N] = x[M,K] . dequant(W)[N,K]^T for one packed [N, K/2] matrix."""
+    M, K = x.shape
+    N = w.shape[-2]
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    _check(lib().matmul_nbits(_p(x), _dt(x), _p(w), _p(scales), _dt(scales), _p(zp), M, N, K,
+                              block_size, _p(y), _stream()), "matmul_nbits")
+    return y
+
+
+def _qw(L, p):
+    return QWeight(L[p + "_w"].data_ptr(), L[p + "_s"].data_ptr(),
+                   None if L.get(p + "_zp") is None else L[p + "_zp"].data_ptr())
+
+
+def qmoe_forward(layer, x=None, out=None, ws=None, accumulate=False, path=PATH_AUTO,
+                 return_routing=False):
+    """The whole layer.  `layer` holds router_w, router_bias, gate_/up_/down_ w, s,
+    zp (device tensors) and ints H, I, E, k, block_size; x [T, H] defaults to
+    layer['x'].  Returns out [T, H] (and (topk_w, topk_ids) if asked)."""
+    L = layer
+    x = L["x"] if x is None else x
+    T = x.shape[0]
+    H, I, E, k, bs = (int(L[n]) for n in ("H", "I", "E", "k", "block_size"))
+    ws = ws or Workspace(T, H, I, E, k, device=x.device)
+    o = out if out is not None else torch.empty((T, H), dtype=x.dtype, device=x.device)
+    tw = ti = None
+    if return_routing:
+        tw = torch.empty((T, k), dtype=torch.float32, device=x.device)
+        ti = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    rc = lib().qmoe_forward_ex(_p(x), _dt(x), _p(L["router_w"]), _p(L.get("router_bias")),
+                               _qw(L, "gate"), _qw(L, "up"), _qw(L, "down"), _dt(L["gate_s"]),
+                               T, H, I, E, k, bs, _p(o), _p(tw), _p(ti), int(bool(accumulate)),
+                               int(path), ws.ptr, ws.nbytes, _stream())
+    _check(rc, "qmoe_forward")
+    return (o, tw, ti) if return_routing else o
+
+
+def qmoe_forward_profiled(layer, events, x=None, out=None, ws=None, path=PATH_AUTO):
+    """qmoe_forward that records torch.cuda.Event objects `events` before the
+    first kernel and after each kernel (kernels serialised)."""
+    L = layer
+    x = L["x"] if x is None else x
+    T = x.shape[0]
+    H, I, E, k, bs = (int(L[n]) for n in ("H", "I", "E", "k", "block_size"))
+    ws = ws or Workspace(T, H, I, E, k, device=x.device)
+    o = out if out is not None else torch.empty((T, H), dtype=x.dtype, device=x.device)
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    rc = lib().qmoe_forward_profiled(_p(x), _dt(x), _p(L["router_w"]), _p(L.get("router_bias")),
+                                     _qw(L, "gate"), _qw(L, "up"), _qw(L, "down"), _dt(L["gate_s"]),
+                                     T, H, I, E, k, bs, _p(o), int(path), ws.ptr, ws.nbytes, _stream(),
+                                     arr, len(events))
+    _check(rc, "qmoe_forward_profiled")
+    return o
+
+
+def qmoe_dequant(w, scales, zp, block_size):
+    """fp32 [N, K] = (q - zp) * scale of one packed [N, K/2] matrix."""
+    N, K2 = w.shape[-2], w.shape[-1]
+    out = torch.empty((N, 2 * K2), dtype=torch.float32, device=w.device)
+    _check(lib().qmoe_dequant(_p(w), _p(scales), _dt(scales), _p(zp), N, 2 * K2, block_size, _p(out),
+                              _stream()), "qmoe_dequant")
+    return out
+
+
+def qmoe_rmsnorm(x, eps=1e-6, out=None):
+    T, H = x.shape
+    o = out if out is not None else torch.empty_like(x)
+    _check(lib().qmoe_rmsnorm(_p(x), _p(o), _dt(x), T, H, float(eps), _stream()), "qmoe_rmsnorm")
+    return o

@@ -1,0 +1,324 @@
+// api.cu -- the C ABI (include/qmoe.h): argument checks on the host, the
+// workspace map, and the launch order of each entry point.  No allocation,
+// no synchronisation (except qmoe_get_device_status, documented blocking).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "launch.h"
+#include "qmoe.h"
+
+using namespace qmoe;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// sm_103 (compute capability 10.3) only; cached per device
+int check_device() {
+  static int ok_cache[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QMOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return QMOE_ERR_UNSUPPORTED;
+  if (!ok_cache[dev]) {
+    int maj = 0, min = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return QMOE_ERR_CUDA;
+    ok_cache[dev] = (maj == 10 && min == 3) ? 1 : 2;
+  }
+  return ok_cache[dev] == 1 ? QMOE_OK : QMOE_ERR_UNSUPPORTED;
+}
+
+bool valid_dtype(int d) { return d == QMOE_F16 || d == QMOE_BF16; }
+bool valid_bs(int bs) { return bs == 32 || bs == 64 || bs == 128; }
+
+int check_qweight(const qmoe_qweight& q, int N, int K, int bs) {
+  if (!q.w || !q.scales) return QMOE_ERR_INVALID_ARG;
+  if (N < 1 || K < 32 || K % 32 || K % bs) return QMOE_ERR_INVALID_ARG;
+  if (!aligned(q.w, 16) || !aligned(q.scales, 2)) return QMOE_ERR_INVALID_ARG;
+  return QMOE_OK;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return QMOE_OK;
+  if (e == cudaErrorInvalidValue) return QMOE_ERR_UNSUPPORTED;  // shape outside the kernel plans
+  return QMOE_ERR_CUDA;
+}
+
+struct Ws {
+  WsLayout L;
+  uint8_t* base;
+  template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+};
+
+int check_route_args(const void* x, const void* router_w, int act_dtype, int T, int H, int E, int k) {
+  if (!x || !router_w) return QMOE_ERR_INVALID_ARG;
+  if (!valid_dtype(act_dtype)) return QMOE_ERR_INVALID_ARG;
+  if (T < 1 || H < 1 || E < 1 || k < 1 || k > E) return QMOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || k > kMaxTopk) return QMOE_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(router_w, 2)) return QMOE_ERR_INVALID_ARG;
+  if ((long long)T * k > (1LL << 30)) return QMOE_ERR_UNSUPPORTED;
+  // router CTA shared memory: x slice of 8 tokens + per-warp partial logits
+  const int split = route_split(T);
+  const int rps = (((H + split - 1) / split) + 7) & ~7;
+  if ((size_t)4 * (8 * rps + 64 * E) > 200 * 1024) return QMOE_ERR_UNSUPPORTED;
+  return QMOE_OK;
+}
+
+int enqueue_route(const Ws& ws, const void* x, const void* router_w, int act_dtype,
+                  const float* bias, int T, int H, int E, int k, float* user_w,
+                  int32_t* user_ids, int32_t* user_offsets, int32_t* user_perm, cudaStream_t st,
+                  bool pdl = true) {
+  RouteParams p = {};
+  p.x = x;
+  p.router_w = router_w;
+  p.bias = bias;
+  p.T = T;
+  p.H = H;
+  p.E = E;
+  p.k = k;
+  p.split = route_split(T);
+  p.rows_per_split = (((H + p.split - 1) / p.split) + 7) & ~7;
+  p.topk_w = ws.at<float>(ws.L.w);
+  p.topk_ids = ws.at<int32_t>(ws.L.ids);
+  p.user_w = user_w;
+  p.user_ids = user_ids;
+  p.offsets = ws.at<int32_t>(ws.L.offsets);
+  p.user_offsets = user_offsets;
+  p.active = ws.at<int32_t>(ws.L.active);
+  p.perm = ws.at<int32_t>(ws.L.perm);
+  p.user_perm = user_perm;
+  p.partial = ws.at<float>(ws.L.partial);
+  p.ctl = ws.at<uint32_t>(ws.L.ctl);
+  return cuda_status(launch_route(p, act_dtype, st, pdl));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qmoe_status_string(int status) {
+  switch (status) {
+    case QMOE_OK: return "ok";
+    case QMOE_ERR_INVALID_ARG: return "invalid argument";
+    case QMOE_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case QMOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case QMOE_ERR_CUDA: return "CUDA runtime error";
+    case QMOE_ERR_TIMEOUT: return "device wait timed out";
+    case QMOE_ERR_DEVICE_CHECK: return "device index check failed";
+    default: return "unknown status";
+  }
+}
+
+size_t qmoe_workspace_size(int T, int H, int I, int E, int k) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
+  return ws_layout(T, H, I, E, k).total;
+}
+
+int qmoe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < kCtlBytes) return QMOE_ERR_WORKSPACE;
+  return cudaMemsetAsync(workspace, 0, kCtlBytes, (cudaStream_t)stream) == cudaSuccess ? QMOE_OK
+                                                                                     : QMOE_ERR_CUDA;
+}
+
+int qmoe_route(const void* x, const void* router_w, int act_dtype, const float* router_bias, int T,
+               int H, int E, int k, float* topk_w, int32_t* topk_ids, int32_t* expert_offsets,
+               int32_t* perm, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_route_args(x, router_w, act_dtype, T, H, E, k);
+  if (rc) return rc;
+  if (!topk_w || !topk_ids) return QMOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, 32, E, k);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
+  if ((rc = check_device())) return rc;
+  Ws ws{L, static_cast<uint8_t*>(workspace)};
+  return enqueue_route(ws, x, router_w, act_dtype, router_bias, T, H, E, k, topk_w, topk_ids,
+                       expert_offsets, perm, (cudaStream_t)stream);
+}
+
+int matmul_nbits(const void* x, int act_dtype, const uint8_t* w, const void* scales,
+                 int scale_dtype, const uint8_t* zp, int M, int N, int K, int block_size, void* y,
+                 void* stream) {
+  if (!x || !y || !valid_dtype(act_dtype) || !valid_dtype(scale_dtype)) return QMOE_ERR_INVALID_ARG;
+  if (!valid_bs(block_size) || M < 1) return QMOE_ERR_INVALID_ARG;
+  qmoe_qweight q{w, scales, zp};
+  int rc = check_qweight(q, N, K, block_size);
+  if (rc) return rc;
+  if (!aligned(x, 16) || !aligned(y, 2)) return QMOE_ERR_INVALID_ARG;
+  if ((rc = check_device())) return rc;
+  // tokens per launch: as many (<= 16) as the kernel's shared-memory plan holds
+  int chunk = M < kDecodeMaxTokens ? M : kDecodeMaxTokens;
+  while (chunk > 0 && !decode_fits(kModeDense, chunk, N, K, block_size, zp != nullptr, 1)) --chunk;
+  if (chunk == 0) return QMOE_ERR_UNSUPPORTED;
+  for (int m0 = 0; m0 < M; m0 += chunk) {
+    const int mt = (M - m0) < chunk ? (M - m0) : chunk;
+    DecodeParams p = {};
+    p.w[0] = w;
+    p.s[0] = scales;
+    p.z[0] = zp;
+    p.N = N;
+    p.K = K;
+    p.bs = block_size;
+    p.nb = K / block_size;
+    p.E = 1;
+    p.k = 1;
+    p.T = mt;
+    p.x16 = static_cast<const uint16_t*>(x) + (size_t)m0 * K;
+    p.out = static_cast<uint16_t*>(y) + (size_t)m0 * N;
+    p.src_row_floats = dec_row_floats(K);
+    rc = cuda_status(launch_decode(p, kModeDense, act_dtype, scale_dtype, zp != nullptr,
+                                   (cudaStream_t)stream, false));
+    if (rc) return rc;
+  }
+  return QMOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int forward_impl(const void* x, int act_dtype, const void* router_w, const float* router_bias,
+                 qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
+                 int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
+                 int32_t* topk_ids_out, int accumulate, int path, void* workspace,
+                 size_t workspace_bytes, void* stream, void* const* events, int n_events) {
+  int rc = check_route_args(x, router_w, act_dtype, T, H, E, k);
+  if (rc) return rc;
+  if (!out || !aligned(out, 16) || !valid_dtype(scale_dtype) || !valid_bs(block_size))
+    return QMOE_ERR_INVALID_ARG;
+  if ((rc = check_qweight(gate, I, H, block_size)) || (rc = check_qweight(up, I, H, block_size)) ||
+      (rc = check_qweight(down, H, I, block_size)))
+    return rc;
+  if ((gate.zp == nullptr) != (up.zp == nullptr)) return QMOE_ERR_INVALID_ARG;
+  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_PREFILL) return QMOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, I, E, k);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
+  if ((rc = check_device())) return rc;
+  const bool zgu = gate.zp != nullptr, zd = down.zp != nullptr;
+  const bool dec_ok = T <= kDecodeMaxTokens && decode_fits(kModeGateUp, T, I, H, block_size, zgu, k) &&
+                      decode_fits(kModeDown, T, H, I, block_size, zd, k);
+  if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
+  if (path == QMOE_PATH_DECODE && !dec_ok) return QMOE_ERR_UNSUPPORTED;
+  if (path == QMOE_PATH_PREFILL) return QMOE_ERR_UNSUPPORTED;  // grouped GEMM path not built yet
+
+  Ws ws{L, static_cast<uint8_t*>(workspace)};
+  cudaStream_t st = (cudaStream_t)stream;
+  // profiling: an event before the first kernel and after each kernel; the
+  // kernels then run back to back without programmatic overlap
+  const bool pdl = events == nullptr;
+  int ev_i = 0;
+  auto mark = [&]() -> int {
+    if (events && ev_i < n_events && events[ev_i])
+      if (cudaEventRecord((cudaEvent_t)events[ev_i], st) != cudaSuccess) return QMOE_ERR_CUDA;
+    ++ev_i;
+    return QMOE_OK;
+  };
+  if ((rc = mark())) return rc;
+  rc = enqueue_route(ws, x, router_w, act_dtype, router_bias, T, H, E, k, topk_w_out, topk_ids_out,
+                     nullptr, nullptr, st, pdl);
+  if (rc || (rc = mark())) return rc;
+
+  DecodeParams g = {};
+  g.w[0] = gate.w; g.s[0] = gate.scales; g.z[0] = gate.zp;
+  g.w[1] = up.w;   g.s[1] = up.scales;   g.z[1] = up.zp;
+  g.N = I; g.K = H; g.bs = block_size; g.nb = H / block_size;
+  g.E = E; g.k = k; g.T = T;
+  g.active = ws.at<int32_t>(L.active);
+  g.offsets = ws.at<int32_t>(L.offsets);
+  g.perm = ws.at<int32_t>(L.perm);
+  g.topk_w = ws.at<float>(L.w);
+  g.x16 = x;
+  g.act_out = ws.at<float>(L.act);
+  g.act_row_floats = dec_row_floats(I);
+  g.src_row_floats = dec_row_floats(H);
+  g.ctl = ws.at<uint32_t>(L.ctl);
+  rc = cuda_status(launch_decode(g, kModeGateUp, act_dtype, scale_dtype, zgu, st, pdl));
+  if (rc || (rc = mark())) return rc;
+
+  DecodeParams d = g;
+  d.w[0] = down.w; d.s[0] = down.scales; d.z[0] = down.zp;
+  d.w[1] = nullptr; d.s[1] = nullptr; d.z[1] = nullptr;
+  d.N = H; d.K = I; d.nb = I / block_size;
+  d.src = ws.at<float>(L.act);
+  d.src_row_floats = dec_row_floats(I);
+  d.x16 = nullptr;
+  d.act_out = nullptr;
+  d.out = out;
+  d.accumulate = accumulate;
+  rc = cuda_status(launch_decode(d, kModeDown, act_dtype, scale_dtype, zd, st, pdl));
+  if (rc) return rc;
+  return mark();
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const float* router_bias,
+                    qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
+                    int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
+                    int32_t* topk_ids_out, int accumulate, int path, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return forward_impl(x, act_dtype, router_w, router_bias, gate, up, down, scale_dtype, T, H, I, E,
+                      k, block_size, out, topk_w_out, topk_ids_out, accumulate, path, workspace,
+                      workspace_bytes, stream, nullptr, 0);
+}
+
+int qmoe_forward_profiled(const void* x, int act_dtype, const void* router_w,
+                          const float* router_bias, qmoe_qweight gate, qmoe_qweight up,
+                          qmoe_qweight down, int scale_dtype, int T, int H, int I, int E, int k,
+                          int block_size, void* out, int path, void* workspace,
+                          size_t workspace_bytes, void* stream, void* const* events,
+                          int n_events) {
+  if (!events || n_events < 1) return QMOE_ERR_INVALID_ARG;
+  return forward_impl(x, act_dtype, router_w, router_bias, gate, up, down, scale_dtype, T, H, I, E,
+                      k, block_size, out, nullptr, nullptr, 0, path, workspace, workspace_bytes,
+                      stream, events, n_events);
+}
+
+int qmoe_forward(const void* x, int act_dtype, const void* router_w, const float* router_bias,
+                 qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
+                 int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
+                 int32_t* topk_ids_out, int accumulate, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  return qmoe_forward_ex(x, act_dtype, router_w, router_bias, gate, up, down, scale_dtype, T, H, I,
+                         E, k, block_size, out, topk_w_out, topk_ids_out, accumulate,
+                         QMOE_PATH_AUTO, workspace, workspace_bytes, stream);
+}
+
+int qmoe_dequant(const uint8_t* w, const void* scales, int scale_dtype, const uint8_t* zp, int N,
+                 int K, int block_size, float* out, void* stream) {
+  if (!out || !valid_dtype(scale_dtype) || !valid_bs(block_size)) return QMOE_ERR_INVALID_ARG;
+  qmoe_qweight q{w, scales, zp};
+  int rc = check_qweight(q, N, K, block_size);
+  if (rc) return rc;
+  if (!aligned(out, 16)) return QMOE_ERR_INVALID_ARG;
+  if ((rc = check_device())) return rc;
+  return cuda_status(launch_dequant(w, scales, scale_dtype, zp, N, K, block_size, out,
+                                    (cudaStream_t)stream));
+}
+
+int qmoe_rmsnorm(const void* x, void* out, int act_dtype, int T, int H, float eps, void* stream) {
+  if (!x || !out || !valid_dtype(act_dtype) || T < 1 || H < 1 || !(eps >= 0.f))
+    return QMOE_ERR_INVALID_ARG;
+  if (!aligned(x, 2) || !aligned(out, 2)) return QMOE_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc) return rc;
+  return cuda_status(launch_rmsnorm(x, out, act_dtype, T, H, eps, (cudaStream_t)stream));
+}
+
+int qmoe_get_device_status(void* workspace, uint32_t* bits_out, void* stream) {
+  if (!workspace) return QMOE_ERR_WORKSPACE;
+  uint32_t bits = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(bits), st) != cudaSuccess)
+    return QMOE_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  if (bits & QMOE_ST_TIMEOUT) return QMOE_ERR_TIMEOUT;
+  if (bits & QMOE_ST_INDEX) return QMOE_ERR_DEVICE_CHECK;
+  return QMOE_OK;
+}
+
+}  // extern "C"

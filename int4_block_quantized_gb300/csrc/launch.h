@@ -1,0 +1,51 @@
+// launch.h -- internal host-side declarations: kernel launchers and the
+// cudaLaunchKernelEx helper (programmatic dependent launch attribute).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "layout.h"
+
+namespace qmoe {
+
+template <typename... Args>
+static inline cudaError_t launch_kernel(void (*fn)(Args...), dim3 grid, dim3 block, size_t smem,
+                                        cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
+// number of SMs of the current device (cached per device)
+int device_sm_count();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per function, device
+// and size (not a stream operation; cached so graph capture sees no calls)
+cudaError_t ensure_smem_ptr(const void* fn, size_t bytes);
+template <typename F>
+static inline cudaError_t ensure_smem(F* fn, size_t bytes) {
+  return ensure_smem_ptr(reinterpret_cast<const void*>(fn), bytes);
+}
+
+cudaError_t launch_route(const RouteParams& p, int act_dtype, cudaStream_t st, bool pdl);
+
+// decode path: returns cudaErrorInvalidValue if the shape does not fit the
+// kernel's shared-memory plan (the caller then reports UNSUPPORTED)
+cudaError_t launch_decode(DecodeParams p, int mode, int act_dtype, int scale_dtype, bool has_zp,
+                          cudaStream_t st, bool pdl);
+bool decode_fits(int mode, int T, int N, int K, int bs, bool has_zp, int k);
+
+cudaError_t launch_dequant(const uint8_t* w, const void* s, int scale_dtype, const uint8_t* zp,
+                           int N, int K, int bs, float* out, cudaStream_t st);
+cudaError_t launch_rmsnorm(const void* x, void* out, int act_dtype, int T, int H, float eps,
+                           cudaStream_t st);
+
+}  // namespace qmoe

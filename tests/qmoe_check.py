@@ -1,0 +1,62 @@
+"""Comparison helpers shared by the GPU parity tests (no method arithmetic).
+
+Tolerance for layer outputs (fp16/bf16 out, fp32 accumulation):
+    |gpu - ref| <= 1e-2 * (1 + |ref|) elementwise.
+Routing: expert ids must equal the oracle's exactly, except for tokens whose
+oracle k-th and (k+1)-th probabilities differ by less than 1e-4 ("near
+ties"); for those the GPU's choice must still be a valid top-k within 1e-4,
+and the output is compared with the oracle re-run on the GPU's routing.
+"""
+import numpy as np
+import torch
+
+TOL = 1e-2
+NEAR_TIE = 1e-4
+
+
+def to_f64(t):
+    return t.detach().float().cpu().double().numpy() if isinstance(t, torch.Tensor) else np.asarray(t, np.float64)
+
+
+def assert_close_layer(got, ref, what=""):
+    got = to_f64(got)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    bound = TOL * (1.0 + np.abs(ref))
+    bad = err > bound
+    assert not bad.any(), "%s: %d elements out of tolerance, worst err %.4g at ref %.4g (max |ref| %.3g)" % (
+        what, int(bad.sum()), float(err.max()), float(ref.flat[int(np.argmax(err - bound))]), float(np.abs(ref).max()))
+    return float((err / (1.0 + np.abs(ref))).max())
+
+
+def near_tie_tokens(probs, k):
+    """Tokens whose k-th and (k+1)-th oracle probabilities are within NEAR_TIE."""
+    s = -np.sort(-probs, axis=1)
+    if probs.shape[1] <= k:
+        return np.zeros(probs.shape[0], dtype=bool)
+    return (s[:, k - 1] - s[:, k]) < NEAR_TIE
+
+
+def check_routing(gpu_ids, gpu_w, probs, ref_ids, k):
+    """Ids bit-exact outside near ties; near-tie choices valid within NEAR_TIE.
+    Returns the boolean mask of near-tie tokens."""
+    gpu_ids = np.asarray(gpu_ids)
+    near = near_tie_tokens(probs, k)
+    for t in range(probs.shape[0]):
+        if not near[t]:
+            assert list(gpu_ids[t]) == list(ref_ids[t]), "token %d: ids %s vs oracle %s" % (
+                t, list(gpu_ids[t]), list(ref_ids[t]))
+        else:
+            s = -np.sort(-probs[t])
+            pk, pk1 = s[k - 1], s[k]
+            chosen = set(int(e) for e in gpu_ids[t])
+            assert len(chosen) == k
+            for e in range(probs.shape[1]):
+                if e in chosen:
+                    assert probs[t, e] >= pk1 - NEAR_TIE
+                else:
+                    assert probs[t, e] <= pk + NEAR_TIE
+    gw = np.asarray(gpu_w, np.float64)
+    pw = np.take_along_axis(probs, gpu_ids.astype(np.int64), axis=1)
+    np.testing.assert_allclose(gw, pw, rtol=1e-5, atol=1e-7)
+    return near
