@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode", choices=list(POOL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool", type=int, default=None,
+                    help="resident weight sets (default: enough that a revisit misses L2); "
+                         "smaller pools only for profiler captures, which flush caches themselves")
     a = ap.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.config]
@@ -217,8 +220,8 @@ def config_dict(wl, a):
         wl.name, wl.T, wl.H, wl.I, wl.E, wl.k, wl.block_size, "bf16" if wl.act_dtype else "fp16",
         "bf16" if wl.scale_dtype else "fp16", "uint4 zero points" if wl.has_zp else "no zero points"),
         "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "block_size": wl.block_size,
-        "pool_layers": POOL[wl.name] if wl.name in POOL else 1,
-        "l2": "weights rotate over %d independent layers (> L2 per revisit); no flush" % POOL.get(wl.name, 1),
+        "pool_layers": a.pool or POOL[wl.name],
+        "l2": "weights rotate over %d independent layers (> L2 per revisit); no flush" % (a.pool or POOL[wl.name]),
         "parallelism": "replicas x%d" % a.gpus}
 
 
@@ -229,7 +232,7 @@ def run_ours(a, wl):
     rank, world, local = dist_init()
     dev = torch.device("cuda", local)
     B.lib()
-    P = POOL[wl.name]
+    P = a.pool or POOL[wl.name]
     layers = [S.make_weights(wl, seed=0, device=dev, layer=l) for l in range(P)]
     xs = [S.make_x(wl, seed=0, device=dev, layer=l) for l in range(P)]
     outs = [torch.empty_like(x) for x in xs]
@@ -289,19 +292,27 @@ def run_ours(a, wl):
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     value = wl.T * a.steps * world / (ms / 1000.0)
 
-    # ---- per-kernel durations (events between kernels, no overlap) for the roofline
+    # ---- per-kernel durations for the roofline: events between the kernels
+    # (no programmatic overlap), replayed from a CUDA graph so host launch
+    # gaps are not measured
     nk = 3
-    dur = [[] for _ in range(nk)]
+    nrep = 3
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(nrep * P)]
     with torch.cuda.stream(s):
-        for rep in range(3):
-            for j in range(P):
-                evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-                B.qmoe_forward_profiled(layers[j], evs, x=xs[j], out=outs[j], ws=ws)
-                if rep > 0:
-                    for kk in range(nk):
-                        dur[kk].append((evs, kk))
+        for evs in evsets:  # torch creates the CUDA event on first record
+            for ev in evs:
+                ev.record(s)
     torch.cuda.synchronize(dev)
-    kms = [statistics.mean(evs[kk].elapsed_time(evs[kk + 1]) for evs, _ in dur[kk]) for kk in range(nk)]
+    g_prof = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_prof, stream=s):
+        for i, evs in enumerate(evsets):
+            j = i % P
+            B.qmoe_forward_profiled(layers[j], evs, x=xs[j], out=outs[j], ws=ws)
+    g_prof.replay()
+    torch.cuda.synchronize(dev)
+    g_prof.replay()
+    torch.cuda.synchronize(dev)
+    kms = [statistics.mean(evs[kk].elapsed_time(evs[kk + 1]) for evs in evsets[P:]) for kk in range(nk)]
     pk = peaks()
     gu_gbs = wb["gateup"] / (kms[1] * 1e-3) / 1e9
 

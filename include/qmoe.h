@@ -85,6 +85,10 @@ typedef struct {
 /* Human-readable name of a status code.  Never NULL. */
 const char* qmoe_status_string(int status);
 
+/* Text of the last CUDA runtime error an entry point on this thread turned
+ * into QMOE_ERR_CUDA / QMOE_ERR_UNSUPPORTED ("no error" if none).  Never NULL. */
+const char* qmoe_last_cuda_error(void);
+
 /* Bytes of device workspace qmoe_route / qmoe_forward need for these
  * shapes (covers both paths).  The workspace is caller-owned, 256-byte
  * aligned device memory.  Before its FIRST use it must be prepared with

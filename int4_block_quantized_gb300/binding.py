@@ -45,6 +45,8 @@ def lib():
         vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         L.qmoe_status_string.restype = ctypes.c_char_p
         L.qmoe_status_string.argtypes = [i32]
+        L.qmoe_last_cuda_error.restype = ctypes.c_char_p
+        L.qmoe_last_cuda_error.argtypes = []
         L.qmoe_workspace_size.restype = sz
         L.qmoe_workspace_size.argtypes = [i32] * 5
         L.qmoe_workspace_init.restype = i32
@@ -86,6 +88,8 @@ def _dt(t):
 
 def _check(rc, where):
     if rc != 0:
+        if rc == 4:
+            where = "%s [%s]" % (where, lib().qmoe_last_cuda_error().decode())
         raise QMoEError(rc, where)
 
 

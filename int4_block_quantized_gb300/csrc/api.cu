@@ -40,8 +40,11 @@ int check_qweight(const qmoe_qweight& q, int N, int K, int bs) {
   return QMOE_OK;
 }
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return QMOE_OK;
+  g_last_cuda_error = e;
   if (e == cudaErrorInvalidValue) return QMOE_ERR_UNSUPPORTED;  // shape outside the kernel plans
   return QMOE_ERR_CUDA;
 }
@@ -89,7 +92,6 @@ int enqueue_route(const Ws& ws, const void* x, const void* router_w, int act_dty
   p.active = ws.at<int32_t>(ws.L.active);
   p.perm = ws.at<int32_t>(ws.L.perm);
   p.user_perm = user_perm;
-  p.partial = ws.at<float>(ws.L.partial);
   p.ctl = ws.at<uint32_t>(ws.L.ctl);
   return cuda_status(launch_route(p, act_dtype, st, pdl));
 }
@@ -109,6 +111,10 @@ const char* qmoe_status_string(int status) {
     case QMOE_ERR_DEVICE_CHECK: return "device index check failed";
     default: return "unknown status";
   }
+}
+
+const char* qmoe_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
 }
 
 size_t qmoe_workspace_size(int T, int H, int I, int E, int k) {

@@ -103,25 +103,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // --------------------------------------------------- packed fp32 (f32x2)
-struct f2 {
-  float x, y;
-};
-__device__ __forceinline__ f2 ffma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0, %1}, rc;\n}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ f2 fsub2(f2 a, f2 b) {
-  f2 d;
-  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " sub.rn.f32x2 ra, ra, rb;\n mov.b64 {%0, %1}, ra;\n}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
+// Native paired fp32 operations of sm_100+ (one instruction for two lanes
+// of work, round-to-nearest-even like the scalar ones).
+using f2 = float2;
+__device__ __forceinline__ f2 ffma2(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ f2 fadd2(f2 a, f2 b) { return __fadd2_rn(a, b); }
 
 // ------------------------------------------------------- warp reductions
 __device__ __forceinline__ float warp_sum(float v) {

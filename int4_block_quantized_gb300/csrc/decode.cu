@@ -11,36 +11,61 @@
 // SwiGLU act = silu(gate) * up from IR guide 3, Expert Computation step 5.
 //
 // GB300 design.  The pages' kernels give one warp per output row and read
-// 4-byte words.  Here every CTA (one per SM) owns a contiguous slice of
-// output rows and walks all selected experts for that slice, so each SM
-// streams the same number of bytes whatever the routing.  A producer warp
-// issues cp.async.bulk copies of whole row slices (contiguous in the
-// [E, N, K/2] layout) plus their scales / zero points into a ring of shared
-// memory stages guarded by mbarriers, so all of a CTA's bytes can be in
-// flight at once.  Consumer warps read 16-byte chunks (32 codes = one 32-wide
-// block), turn nibble j of each 16-bit half into the exact float
-// (q - zp) * 16^j with one LOP3 and one packed subtract (magic exponent
-// 2^23), and FMA with activations pre-scaled by 16^-j (fma.rn.f32x2), all
-// in fp32.  Work is grouped per distinct expert, so every weight byte is
-// read once per call even when several tokens chose the same expert.
+// 4-byte words.  Here one CTA per SM streams an equal share of the selected
+// experts' bytes:
+//  * gate-up and the dense GEMV split the flattened (expert, row) space into
+//    equal contiguous ranges, so a CTA's rows are one or two large
+//    contiguous slices ("stages") of the [E, N, K/2] tensors;
+//  * down gives each CTA a fixed slice of output rows across every selected
+//    expert, so the weighted sum over the k experts stays inside the CTA
+//    (deterministic, no atomics).
+// A producer warp issues cp.async.bulk copies of each stage's rows, block
+// scales and zero points into a ring of shared-memory slots guarded by
+// mbarriers, the copies of a whole ring-full at once across its lanes.
+// Consumer warps take (stage, 4-row group) work items, so different warps
+// work on different stages concurrently.  A lane owns two adjacent 16-byte
+// chunks (64 codes) of a row; nibble j of each 16-bit half-word becomes the
+// exact float (q - zp) * 16^j with one three-input LOP3 (nibble OR-ed into
+// the mantissa of 2^23) and half a packed subtract, and is multiplied with
+// activations pre-scaled by 16^-j in packed fp32 FMAs (fma.rn.f32x2); all
+// accumulation is fp32.  Work is grouped per distinct expert, so every
+// weight byte is read once per call even when several tokens chose the
+// same expert.
 #include <math.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
 
 namespace qmoe {
 
-constexpr int kCW = 16;                         // consumer warps
+constexpr int kCW = 11;                         // consumer warps
 constexpr int kDecodeThreads = (kCW + 1) * 32;  // + one producer warp
-constexpr int kMaxSlots = 16;
-constexpr uint32_t kFixedSmem = 3584;           // barriers, stage headers, routing copy
+constexpr int kMaxSlots = 8;
+// rows per work item for NT tokens and NMAT matrices (register budget:
+// at most 4 rows x tokens x matrices partial sums, x chunks in registers)
+__host__ __device__ constexpr int rows_per_item(int nt, int nmat) {
+  return nmat == 2 ? (nt == 1 ? 2 : 1) : (nt == 1 ? 4 : (nt == 2 ? 2 : 1));
+}
+constexpr int kJobsPerStage = 10;               // W,S,Z of two matrices + 4 activation rows
 constexpr uint32_t kSmemBudget = 232448;        // 227 KB dynamic shared memory
 
-struct SlotHdr {
-  int e, ntok, ph[4];  // ph: alignment phase of scales0, scales1, zp0, zp1 images
-  int a[kTokGroup], t[kTokGroup];
+// One stage: rows [row0, row0 + nrows) of expert e's matrices and the
+// tokens (assignments perm[pbase .. pbase + ntok)) they serve.
+struct StageEnt {
+  int e, pbase, ntok, row0, nrows;
+  int ph[4];  // alignment phase of the scales0, scales1, zp0, zp1 images
+  int pad[3];
 };
-static_assert(sizeof(SlotHdr) <= 64, "stage header must fit 64 bytes");
+static_assert(sizeof(StageEnt) == 48, "stage entry is 48 bytes");
+
+// fixed shared-memory carve (bytes); the stage table follows at kFixedSmem
+constexpr uint32_t kOffActive = 256;
+constexpr uint32_t kOffOff = kOffActive + 4 * (kMaxExperts + 2);
+constexpr uint32_t kOffPerm = kOffOff + 4 * (kMaxExperts + 2);
+constexpr uint32_t kOffWt = kOffPerm + 4 * kDecodeMaxTokens * kMaxTopk;
+constexpr uint32_t kFixedSmem = (kOffWt + 4 * kDecodeMaxTokens * kMaxTopk + 127) & ~127u;
 
 struct SlotLayout {
   uint32_t w[2], s[2], z[2], act, bytes;
@@ -71,335 +96,472 @@ __host__ __device__ inline SlotLayout slot_layout(int mode, int rows, int K, int
   return L;
 }
 
-// Producer-warp copy of `bytes` global bytes into shared memory at
-// dst_base + (src mod 16): the 16-byte-aligned middle goes by bulk copy
-// (counted on `bar`), the ragged head / tail bytes by plain loads.
-// Returns the phase (src mod 16).  Lane 0 must have added body bytes to the
-// barrier's expected transaction count (see body_bytes()).
-__device__ __forceinline__ uint32_t body_bytes(const void* src, uint32_t bytes) {
-  const uint32_t ph = (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u);
-  const uint32_t head = min(bytes, (16u - ph) & 15u);
-  return (bytes - head) & ~15u;
+// Shared-memory plan of one launch (host and device agree on it).
+struct DecodePlan {
+  int grid;        // CTAs
+  int rows_cta;    // gate-up / dense: rows of the flattened space per CTA (max); down: slice rows (max)
+  int slot_rows;   // rows per stage slot
+  int max_stages;  // stage-table entries per CTA
+  int nslots;
+  uint32_t res_off, stage_off, slot_base, smem;
+};
+
+// ---------------------------------------------------------------- dequant
+// A register the compiler cannot fold back into an immediate, so that
+// (v & MASK) | magic is a single three-input LOP3.
+__device__ __forceinline__ uint32_t opaque(uint32_t v) {
+  asm volatile("mov.b32 %0, %1;" : "=r"(v) : "r"(v));
+  return v;
 }
-__device__ __forceinline__ int stage_bytes(uint8_t* dst_base, const uint8_t* src, uint32_t bytes,
-                                           uint64_t* bar, int lane) {
+template <uint32_t MASK>
+__device__ __forceinline__ float or_masked(uint32_t v, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(v), "n"(MASK), "r"(magic));  // (v & m) | c
+  return __uint_as_float(d);
+}
+
+// -(2^23 + zp * 16^j) for nibble positions j = 0..3 of a half-word.
+struct ZConst {
+  f2 c01, c23;
+};
+__device__ __forceinline__ ZConst zconst(uint32_t zp, uint32_t neg_magic) {
+  const uint32_t z = zp * 0x1111u;
+  return ZConst{make_float2(or_masked<0xFu>(z, neg_magic), or_masked<0xF0u>(z, neg_magic)),
+                make_float2(or_masked<0xF00u>(z, neg_magic), or_masked<0xF000u>(z, neg_magic))};
+}
+
+// Dequantise one 16-byte chunk (32 codes) into 16 float pairs holding
+// (q - zp) * 16^j, j = position of the nibble in its 16-bit half-word:
+// 2^23 + q * 16^j is the nibble OR-ed into the mantissa of 2^23 (one LOP3),
+// and 2^23 + zp * 16^j is subtracted by a packed add.  Every value is an
+// exact integer times a power of two.
+__device__ __forceinline__ void dequant_chunk(const uint4 q, const ZConst zc, uint32_t magic,
+                                              f2 (&wv)[16]) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = qw[i], hi = qw[i] >> 16;
+    wv[4 * i + 0] = fadd2(make_float2(or_masked<0xFu>(lo, magic), or_masked<0xF0u>(lo, magic)), zc.c01);
+    wv[4 * i + 1] = fadd2(make_float2(or_masked<0xF00u>(lo, magic), or_masked<0xF000u>(lo, magic)), zc.c23);
+    wv[4 * i + 2] = fadd2(make_float2(or_masked<0xFu>(hi, magic), or_masked<0xF0u>(hi, magic)), zc.c01);
+    wv[4 * i + 3] = fadd2(make_float2(or_masked<0xF00u>(hi, magic), or_masked<0xF000u>(hi, magic)), zc.c23);
+  }
+}
+
+// 32 activations of one chunk (decode layout: 8 float4 strided by 32).
+struct XChunk {
+  float4 v[8];
+};
+__device__ __forceinline__ void load_x(const float4* xr, XChunk& x) {
+#pragma unroll
+  for (int f = 0; f < 8; ++f) x.v[f] = xr[f * 32];
+}
+// fp32 dot of a dequantised chunk with its activations (4 packed chains).
+__device__ __forceinline__ float chunk_dot(const f2 (&wv)[16], const XChunk& x) {
+  f2 d0 = make_float2(0.f, 0.f), d1 = d0, d2 = d0, d3 = d0;
+#pragma unroll
+  for (int f = 0; f < 8; f += 2) {
+    d0 = ffma2(wv[2 * f], make_float2(x.v[f].x, x.v[f].y), d0);
+    d1 = ffma2(wv[2 * f + 1], make_float2(x.v[f].z, x.v[f].w), d1);
+    d2 = ffma2(wv[2 * f + 2], make_float2(x.v[f + 1].x, x.v[f + 1].y), d2);
+    d3 = ffma2(wv[2 * f + 3], make_float2(x.v[f + 1].z, x.v[f + 1].w), d3);
+  }
+  const f2 d = fadd2(fadd2(d0, d1), fadd2(d2, d3));
+  return d.x + d.y;
+}
+
+// Dense `Rows` x NT dot products of one work item: rows [rb, rb + nr) of the
+// stage's matrices (NMAT = 2: gate and up) against NT activation rows.
+// acc[m][r][j] gets lane-partial sums (fp32) to be reduced across the warp.
+template <int NMAT, int NT, int RG, typename TS, bool HAS_ZP>
+__device__ __forceinline__ void item_dot(const uint8_t* slot, const SlotLayout& SL, const StageEnt& st,
+                                         int rb, int nr, const float4* const (&xr)[kTokGroup],
+                                         int K, int nb, int bshift, uint32_t magic, uint32_t neg_magic,
+                                         const ZConst zfixed, int lane, float (&acc)[NMAT][RG][NT]) {
+  const int nchunks = K / 32;
+  const int row_bytes = K / 2;
+#pragma unroll
+  for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+    for (int r = 0; r < RG; ++r)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) acc[m][r][j] = 0.f;
+  // the lane's two adjacent chunks, one at a time (one activation chunk live)
+  for (int c = 2 * lane; c < nchunks; c += (c & 1) ? 63 : 1) {
+    const int blk = c >> bshift;
+    const int xo = (c >> 6) * 512 + (c & 1) * 256 + lane;  // float4 index of (s, u, f = 0)
+    XChunk xa;
+    if (NT == 1) load_x(xr[0] + xo, xa);
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+      if (r < nr) {
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const uint8_t* wrow = slot + SL.w[m] + (size_t)(rb + r) * row_bytes + c * 16;
+          const uint16_t* srow = reinterpret_cast<const uint16_t*>(slot + SL.s[m] + st.ph[m]) + (size_t)(rb + r) * nb;
+          const uint8_t* zrow = slot + SL.z[m] + st.ph[2 + m] + (size_t)(rb + r) * nb;
+          f2 wv[16];
+          const uint4 q = *reinterpret_cast<const uint4*>(wrow);
+          const float sc = Half<TS>::to_float(srow[blk]);
+          dequant_chunk(q, HAS_ZP ? zconst(zrow[blk], neg_magic) : zfixed, magic, wv);
+          if (NT == 1) {
+            acc[m][r][0] = fmaf(sc, chunk_dot(wv, xa), acc[m][r][0]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              XChunk xj;
+              load_x(xr[j] + xo, xj);
+              acc[m][r][j] = fmaf(sc, chunk_dot(wv, xj), acc[m][r][j]);
+            }
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+    for (int r = 0; r < RG; ++r)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) acc[m][r][j] = warp_sum(acc[m][r][j]);
+}
+
+// ---------------------------------------------------------------- producer
+// Copy `bytes` global bytes into shared memory at dst_base + (src mod 16):
+// the 16-byte-aligned middle by bulk copy (expected bytes registered on `bar`
+// first), the ragged head / tail (< 16 bytes each) by plain loads.  One
+// lane does all of it; returns src mod 16.
+__device__ __forceinline__ int copy_ragged(uint8_t* dst_base, const uint8_t* src, uint32_t bytes,
+                                           uint64_t* bar) {
   const uint32_t ph = (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u);
   const uint32_t head = min(bytes, (16u - ph) & 15u);
   const uint32_t body = (bytes - head) & ~15u;
   const uint32_t tail = bytes - head - body;
   uint8_t* dst = dst_base + ph;
-  if (lane == 0 && body) bulk_g2s(dst + head, src + head, body, bar);
-  if ((uint32_t)lane < head) dst[lane] = __ldg(src + lane);
-  if ((uint32_t)lane < tail) dst[head + body + lane] = __ldg(src + head + body + lane);
+  if (body) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(body) : "memory");
+    bulk_g2s(dst + head, src + head, body, bar);
+  }
+  for (uint32_t i = 0; i < head; ++i) dst[i] = __ldg(src + i);
+  for (uint32_t i = 0; i < tail; ++i) dst[head + body + i] = __ldg(src + head + body + i);
   return (int)ph;
 }
 
-// One output row against up to kTokGroup activation rows (decode layout).
-// wrow: 16-byte chunks of packed codes; srow / zrow: the row's block scales
-// and zero points; xs[j]: activation row j.  acc[j] += row . x_j (fp32).
-template <typename TS, bool HAS_ZP>
-__device__ __forceinline__ void row_dot(const uint8_t* wrow, const uint16_t* srow,
-                                        const uint8_t* zrow, int nchunks, int bshift,
-                                        const float* const* xs, int ntok, float* acc, int lane) {
-  constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
-  for (int c = lane; c < nchunks; c += 32) {
-    const uint4 q = *reinterpret_cast<const uint4*>(wrow + c * 16);
-    const int blk = c >> bshift;
-    const float s = Half<TS>::to_float(srow[blk]);
-    const float z = HAS_ZP ? (float)zrow[blk] : 8.f;
-    const f2 c01 = {8388608.f + z, fmaf(z, 16.f, 8388608.f)};
-    const f2 c23 = {fmaf(z, 256.f, 8388608.f), fmaf(z, 4096.f, 8388608.f)};
-    f2 wv[16];
-    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+__device__ __forceinline__ void copy_bulk(uint8_t* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+  bulk_g2s(dst, src, bytes, bar);
+}
+
+template <int MODE, int NT, typename TS, typename TA, bool HAS_ZP>
+__device__ __forceinline__ void run_item(const DecodeParams& p, const uint8_t* slot, const SlotLayout& SL,
+                                         const StageEnt& st, int s, int g, int tg, const int* s_perm,
+                                         const float* res, float* partial, int kdec, int bshift,
+                                         uint32_t magic, uint32_t neg_magic, const ZConst zfixed,
+                                         int lane) {
+  constexpr int NMAT = (MODE == kModeGateUp) ? 2 : 1;
+  constexpr int RG = rows_per_item(NT, NMAT);
+  const int rb = g * RG;
+  const int nr = min(RG, st.nrows - rb);
+  const int j0 = tg * kTokGroup;
+  // activation rows of the item's tokens
+  const float4* xr[kTokGroup];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = qw[i], vh = qw[i] >> 16;
-      wv[4 * i + 0] = fsub2({__uint_as_float(kMagic | (v & 0xFu)), __uint_as_float(kMagic | (v & 0xF0u))}, c01);
-      wv[4 * i + 1] = fsub2({__uint_as_float(kMagic | (v & 0xF00u)), __uint_as_float(kMagic | (v & 0xF000u))}, c23);
-      wv[4 * i + 2] = fsub2({__uint_as_float(kMagic | (vh & 0xFu)), __uint_as_float(kMagic | (vh & 0xF0u))}, c01);
-      wv[4 * i + 3] = fsub2({__uint_as_float(kMagic | (vh & 0xF00u)), __uint_as_float(kMagic | (vh & 0xF000u))}, c23);
+  for (int j = 0; j < kTokGroup; ++j) {
+    const int jj = j < NT ? j : 0;
+    if (MODE == kModeDown) {
+      xr[j] = reinterpret_cast<const float4*>(slot + SL.act) + (size_t)(j0 + jj) * (p.src_row_floats / 4);
+    } else {
+      const int a = (MODE == kModeDense) ? (st.pbase + j0 + jj) : s_perm[st.pbase + j0 + jj];
+      const int t = (MODE == kModeDense) ? a : a / p.k;
+      xr[j] = reinterpret_cast<const float4*>(res) + (size_t)t * (kdec / 4);
     }
-    const int xo = ((c >> 5) * 8) * 32 + (c & 31);  // float4 index of f = 0
+  }
+  float acc[NMAT][RG][NT];
+  item_dot<NMAT, NT, RG, TS, HAS_ZP>(slot, SL, st, rb, nr, xr, p.K, p.nb, bshift, magic, neg_magic,
+                                     zfixed, lane, acc);
+  // epilogue: one output per lane (lane = r * NT + j)
+  const int r = lane / NT, j = lane - r * NT;
+  if (r < nr && r < RG) {
+    float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < kTokGroup; ++j) {
-      if (j < ntok) {
-        const float4* xr = reinterpret_cast<const float4*>(xs[j]) + xo;
-        f2 d0 = {0.f, 0.f}, d1 = {0.f, 0.f}, d2 = {0.f, 0.f}, d3 = {0.f, 0.f};
+    for (int rr = 0; rr < RG; ++rr)
 #pragma unroll
-        for (int f = 0; f < 8; f += 2) {
-          const float4 xa = xr[f * 32];
-          const float4 xb = xr[(f + 1) * 32];
-          d0 = ffma2(wv[2 * f], {xa.x, xa.y}, d0);
-          d1 = ffma2(wv[2 * f + 1], {xa.z, xa.w}, d1);
-          d2 = ffma2(wv[2 * f + 2], {xb.x, xb.y}, d2);
-          d3 = ffma2(wv[2 * f + 3], {xb.z, xb.w}, d3);
+      for (int jj = 0; jj < NT; ++jj)
+        if (rr == r && jj == j) {
+          v0 = acc[0][rr][jj];
+          v1 = acc[NMAT - 1][rr][jj];
         }
-        const float dot = ((d0.x + d0.y) + (d1.x + d1.y)) + ((d2.x + d2.y) + (d3.x + d3.y));
-        acc[j] = fmaf(s, dot, acc[j]);
-      }
+    if (MODE == kModeGateUp) {
+      const int a = s_perm[st.pbase + j0 + j];
+      const int i = st.row0 + rb + r;
+      const float act = v0 / (1.f + expf(-v0)) * v1;
+      p.act_out[(size_t)a * p.act_row_floats + dec_index(i)] = act * dec_prescale(i);
+    } else if (MODE == kModeDense) {
+      const int t = st.pbase + j0 + j;
+      static_cast<uint16_t*>(p.out)[(size_t)t * p.N + st.row0 + rb + r] = Half<TA>::from_float(v0);
+    } else {
+      partial[((size_t)s * kTokGroup + j) * st.nrows + rb + r] = v0;
     }
   }
 }
 
-// Stage iterator: (d-th active expert, first token of the group).
-struct StageIt {
-  int d, g0;
-};
-
 template <int MODE, typename TS, typename TA, bool HAS_ZP>
-__global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(DecodeParams p, DecodePlan P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxSlots;
-  SlotHdr* hdr = reinterpret_cast<SlotHdr*>(smem + 256);
-  int* s_active = reinterpret_cast<int*>(smem + 256 + 64 * kMaxSlots);  // [0]=D, [1..D]
-  int* s_off = s_active + (kMaxExperts + 2);                             // [E+1]
-  float* res = reinterpret_cast<float*>(smem + kFixedSmem);
-  uint8_t* slots = smem + p.slot_base;
+  uint64_t* route_bar = empty + kMaxSlots;
+  int* s_nst = reinterpret_cast<int*>(route_bar + 1);
+  int* s_active = reinterpret_cast<int*>(smem + kOffActive);  // [0]=D, [1..D]
+  int* s_off = reinterpret_cast<int*>(smem + kOffOff);        // [E+1]
+  int* s_perm = reinterpret_cast<int*>(smem + kOffPerm);      // [T*k]
+  float* s_wt = reinterpret_cast<float*>(smem + kOffWt);      // [T*k] routing weights (down)
+  float* res = reinterpret_cast<float*>(smem + P.res_off);    // x rows (gate-up / dense) or partials (down)
+  StageEnt* s_stage = reinterpret_cast<StageEnt*>(smem + P.stage_off);
+  uint8_t* slots = smem + P.slot_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint32_t* status = p.ctl ? p.ctl + kCtlStatus : nullptr;
   const int N = p.N, K = p.K, nb = p.nb;
+  const int NS = P.nslots;
+  const SlotLayout SL = slot_layout(MODE, P.slot_rows, K, nb, HAS_ZP, p.src_row_floats, p.T);
+  const int kdec = dec_row_floats(K);
+  // down: a fixed slice of output rows; gate-up / dense: a range of the
+  // flattened (expert, row) space
   const int r0 = (int)(((long long)blockIdx.x * N) / gridDim.x);
   const int r1 = (int)(((long long)(blockIdx.x + 1) * N) / gridDim.x);
-  const int nrows = r1 - r0;
-  const int NS = p.nslots;
-  const SlotLayout SL = slot_layout(MODE, p.rows_per_cta_max, K, nb, HAS_ZP, p.src_row_floats, p.T);
-  const int kdec = dec_row_floats(K);
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 32);
       mbar_init(&empty[i], kCW);
     }
+    mbar_init(route_bar, 32);
     fence_barrier_init();
   }
-  // activations resident for the whole kernel (gate-up / dense)
-  if (MODE != kModeDown) {
-    const uint16_t* x = static_cast<const uint16_t*>(p.x16);
-    const int n = p.T * K;
-    for (int i = tid; i < n; i += kDecodeThreads) {
-      const int t = i / K, kk = i - t * K;
-      res[t * kdec + dec_index(kk)] = Half<TA>::to_float(x[i]) * dec_prescale(kk);
-    }
-  } else {
-    for (int i = tid; i < p.T * p.rows_per_cta_max; i += kDecodeThreads) res[i] = 0.f;
-  }
-  // routing (written by the router; for down, complete before this grid starts)
-  if (MODE == kModeGateUp) pdl_wait();
-  if (MODE == kModeDense) {
-    if (tid == 0) {
-      s_active[0] = 1;
-      s_active[1] = 0;
-      s_off[0] = 0;
-      s_off[1] = p.T;
-    }
-  } else {
-    for (int i = tid; i <= p.E; i += kDecodeThreads) s_off[i] = p.offsets[i];
-    const int D = p.active[0];
-    for (int i = tid; i <= D; i += kDecodeThreads) s_active[i] = p.active[i];
-  }
   __syncthreads();
-  if (MODE == kModeGateUp) pdl_trigger();
-  const int D = s_active[0];
-
-  auto n_of = [&](int d) {
-    const int e = s_active[1 + d];
-    return s_off[e + 1] - s_off[e];
-  };
 
   if (warp == kCW) {
-    // ------------------------------------------------------------ producer
-    const int nmat = (MODE == kModeGateUp) ? 2 : 1;
-    bool waited = (MODE != kModeDown);
-    StageIt it = {0, 0};
-    int stage = 0;
-    // Down: weights of the first ring-full of stages go out before the
-    // previous grid (gate-up, which writes act) has finished.
-    int deferred_begin = -1, deferred_end = -1;
-    StageIt deferred_it = it;
-    for (; it.d < D; ++stage) {
-      const int slot = stage % NS;
-      const int round = stage / NS;
-      if (round > 0) {
-        if (!waited) {
-          // flush the deferred activation copies before reusing a slot
-          pdl_wait();
-          waited = true;
-          StageIt jt = deferred_it;
-          for (int s2 = deferred_begin; s2 < deferred_end; ++s2) {
-            const int sl = s2 % NS;
-            const int n = n_of(jt.d), nt = min(kTokGroup, n - jt.g0);
-            for (int j = 0; j < nt; ++j)
-              if (lane == 0)
-                bulk_g2s(slots + sl * SL.bytes + SL.act + (uint32_t)j * p.src_row_floats * 4,
-                         p.src + (size_t)hdr[sl].a[j] * p.src_row_floats, p.src_row_floats * 4u,
-                         &full[sl]);
-            __syncwarp();
-            mbar_arrive(&full[sl]);
-            jt.g0 += kTokGroup;
-            if (jt.g0 >= n) { ++jt.d; jt.g0 = 0; }
-          }
-        }
-        if (!mbar_wait(&empty[slot], (round - 1) & 1, status)) break;
-      }
-      const int e = s_active[1 + it.d];
-      const int n = n_of(it.d);
-      const int ntok = min(kTokGroup, n - it.g0);
-      uint8_t* sb = slots + slot * SL.bytes;
-      // stage header
-      if (lane == 0) {
-        hdr[slot].e = e;
-        hdr[slot].ntok = ntok;
-      }
-      if (lane < ntok) {
-        const int a = (MODE == kModeDense) ? (it.g0 + lane) : p.perm[s_off[e] + it.g0 + lane];
-        hdr[slot].a[lane] = a;
-        hdr[slot].t[lane] = (MODE == kModeDense) ? a : a / p.k;
-      }
-      // expected transaction bytes
-      uint32_t tx = 0;
-      const size_t row0 = (size_t)e * N + r0;
-      for (int m = 0; m < nmat; ++m) {
-        tx += (uint32_t)nrows * (K / 2);
-        tx += body_bytes(static_cast<const uint8_t*>(p.s[m]) + row0 * nb * 2, (uint32_t)nrows * nb * 2);
-        if (HAS_ZP) tx += body_bytes(p.z[m] + row0 * nb, (uint32_t)nrows * nb);
-      }
-      if (MODE == kModeDown) tx += (uint32_t)ntok * p.src_row_floats * 4;
-      if (lane == 0) asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&full[slot])), "r"(tx) : "memory");
+    // ================================================================ producer
+    // 1. routing -> shared memory (one round trip), then the stage table
+    if (MODE == kModeGateUp) pdl_wait();
+    int nst = 0;
+    if (MODE != kModeDense) {
+      const int A = p.T * p.k;
+      for (int i = lane; i <= p.E; i += 32) s_off[i] = __ldcg(p.offsets + i);
+      for (int i = lane; i <= p.E; i += 32) s_active[i] = __ldcg(p.active + i);
+      for (int i = lane; i < A; i += 32) s_perm[i] = __ldcg(p.perm + i);
+      if (MODE == kModeDown)
+        for (int i = lane; i < A; i += 32) s_wt[i] = __ldcg(p.topk_w + i);
       __syncwarp();
-      for (int m = 0; m < nmat; ++m) {
-        if (lane == 0) bulk_g2s(sb + SL.w[m], p.w[m] + row0 * (K / 2), (uint32_t)nrows * (K / 2), &full[slot]);
-        const int phs = stage_bytes(sb + SL.s[m], static_cast<const uint8_t*>(p.s[m]) + row0 * nb * 2,
-                                    (uint32_t)nrows * nb * 2, &full[slot], lane);
-        int phz = 0;
-        if (HAS_ZP) phz = stage_bytes(sb + SL.z[m], p.z[m] + row0 * nb, (uint32_t)nrows * nb, &full[slot], lane);
-        if (lane == 0) {
-          hdr[slot].ph[m] = phs;
-          hdr[slot].ph[2 + m] = phz;
-        }
-      }
-      __syncwarp();
-      if (MODE == kModeDown && !waited) {
-        if (deferred_begin < 0) {
-          deferred_begin = stage;
-          deferred_it = it;
-        }
-        deferred_end = stage + 1;
-      } else {
-        if (MODE == kModeDown) {
-          for (int j = 0; j < ntok; ++j)
-            if (lane == 0)
-              bulk_g2s(sb + SL.act + (uint32_t)j * p.src_row_floats * 4,
-                       p.src + (size_t)hdr[slot].a[j] * p.src_row_floats, p.src_row_floats * 4u,
-                       &full[slot]);
-          __syncwarp();
-        }
-        mbar_arrive(&full[slot]);
-      }
-      it.g0 += kTokGroup;
-      if (it.g0 >= n) { ++it.d; it.g0 = 0; }
     }
-    if (!waited) {
-      pdl_wait();
-      StageIt jt = deferred_it;
-      for (int s2 = deferred_begin; s2 >= 0 && s2 < deferred_end; ++s2) {
-        const int sl = s2 % NS;
-        const int n = n_of(jt.d), nt = min(kTokGroup, n - jt.g0);
-        for (int j = 0; j < nt; ++j)
-          if (lane == 0)
-            bulk_g2s(slots + sl * SL.bytes + SL.act + (uint32_t)j * p.src_row_floats * 4,
-                     p.src + (size_t)hdr[sl].a[j] * p.src_row_floats, p.src_row_floats * 4u, &full[sl]);
-        __syncwarp();
-        mbar_arrive(&full[sl]);
-        jt.g0 += kTokGroup;
-        if (jt.g0 >= n) { ++jt.d; jt.g0 = 0; }
+    if (MODE == kModeDown) {
+      // stage = (expert, up to kTokGroup of its assignments) over this CTA's slice
+      const int D = s_active[0];
+      for (int d0 = 0; d0 < D; d0 += 32) {
+        const int d = d0 + lane;
+        int e = 0, n = 0, g = 0;
+        if (d < D) {
+          e = s_active[1 + d];
+          n = s_off[e + 1] - s_off[e];
+          g = (n + kTokGroup - 1) / kTokGroup;
+        }
+        int incl = g;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int base = nst + incl - g;
+        for (int gi = 0; gi < g && base + gi < P.max_stages; ++gi) {
+          StageEnt& se = s_stage[base + gi];
+          se.e = e;
+          se.pbase = s_off[e] + gi * kTokGroup;
+          se.ntok = min(kTokGroup, n - gi * kTokGroup);
+          se.row0 = r0;
+          se.nrows = r1 - r0;
+        }
+        nst += __shfl_sync(0xffffffffu, incl, 31);
       }
+    } else if (lane == 0) {
+      // equal contiguous ranges of the flattened (expert, row) space, cut at
+      // expert boundaries and at slot_rows
+      const int D = (MODE == kModeDense) ? 1 : s_active[0];
+      const long long F = (long long)D * N;
+      const long long f0 = (long long)blockIdx.x * F / gridDim.x, f1 = (long long)(blockIdx.x + 1) * F / gridDim.x;
+      for (long long f = f0; f < f1 && nst < P.max_stages;) {
+        const int d = (int)(f / N), i0 = (int)(f - (long long)d * N);
+        const int n = (int)min((long long)min(N - i0, P.slot_rows), f1 - f);
+        StageEnt& se = s_stage[nst++];
+        se.e = (MODE == kModeDense) ? 0 : s_active[1 + d];
+        se.pbase = (MODE == kModeDense) ? 0 : s_off[se.e];
+        se.ntok = (MODE == kModeDense) ? p.T : s_off[se.e + 1] - s_off[se.e];
+        se.row0 = i0;
+        se.nrows = n;
+        f += n;
+      }
+    }
+    nst = __shfl_sync(0xffffffffu, nst, 0);
+    if (MODE == kModeDown) nst = min(nst, P.max_stages);
+    if (lane == 0) *s_nst = nst;
+    __syncwarp();
+    mbar_arrive(route_bar);  // release: routing and stage table
+    if (MODE == kModeGateUp) pdl_trigger();
+
+    const int nmat = (MODE == kModeGateUp) ? 2 : 1;
+    // copies of stages [sa, sb): job = (stage, kind), lane-parallel
+    auto issue = [&](int sa, int sb, bool weights, bool acts) {
+      const int total = (sb - sa) * kJobsPerStage;
+      for (int jid = lane; jid < total; jid += 32) {
+        const int s = sa + jid / kJobsPerStage, job = jid % kJobsPerStage;
+        const int slot = s % NS;
+        StageEnt& st = s_stage[s];
+        uint8_t* sb_ = slots + slot * SL.bytes;
+        uint64_t* bar = &full[slot];
+        const size_t row0 = (size_t)st.e * N + st.row0;
+        if (job < 6) {
+          const int m = job / 3, kind = job % 3;
+          if (!weights || m >= nmat || (kind == 2 && !HAS_ZP)) continue;
+          // (select, not index: a runtime index would put the layout in local memory)
+          const uint32_t ow = m ? SL.w[1] : SL.w[0], os = m ? SL.s[1] : SL.s[0], oz = m ? SL.z[1] : SL.z[0];
+          if (kind == 0) {
+            copy_bulk(sb_ + ow, (m ? p.w[1] : p.w[0]) + row0 * (K / 2), (uint32_t)st.nrows * (K / 2), bar);
+          } else if (kind == 1) {
+            st.ph[m] = copy_ragged(sb_ + os, static_cast<const uint8_t*>(m ? p.s[1] : p.s[0]) + row0 * nb * 2,
+                                   (uint32_t)st.nrows * nb * 2, bar);
+          } else {
+            st.ph[2 + m] = copy_ragged(sb_ + oz, (m ? p.z[1] : p.z[0]) + row0 * nb, (uint32_t)st.nrows * nb, bar);
+          }
+        } else if (MODE == kModeDown && acts) {
+          const int j = job - 6;
+          if (j >= st.ntok) continue;
+          const int a = s_perm[st.pbase + j];
+          copy_bulk(sb_ + SL.act + (uint32_t)j * p.src_row_floats * 4, p.src + (size_t)a * p.src_row_floats,
+                    p.src_row_floats * 4u, bar);
+        }
+      }
+    };
+    auto arrive = [&](int sa, int sb) {
+      __syncwarp();
+      for (int s = sa; s < sb; ++s) mbar_arrive(&full[s % NS]);
+    };
+    // 2. first ring-full: every copy in flight at once.  For down, the
+    //    activation rows come from the previous grid (gate-up): the weights
+    //    go out before waiting for it.
+    const int n0 = min(NS, nst);
+    issue(0, n0, true, MODE != kModeDown);
+    if (MODE == kModeDown) {
+      pdl_wait();
+      issue(0, n0, false, true);
+    }
+    arrive(0, n0);
+    // 3. refill slots as consumers release them
+    bool ok = true;
+    for (int s = n0; s < nst; ++s) {
+      ok = mbar_wait(&empty[s % NS], ((s / NS) - 1) & 1, status);
+      if (!ok) break;
+      issue(s, s + 1, true, true);
+      arrive(s, s + 1);
     }
     // drain: do not exit while bulk copies into this CTA's smem are in flight
-    for (int s2 = max(0, stage - NS); s2 < stage; ++s2)
-      if (!mbar_wait(&full[s2 % NS], (s2 / NS) & 1, status)) break;
+    if (ok)
+      for (int s = max(0, nst - NS); s < nst; ++s)
+        if (!mbar_wait(&full[s % NS], (s / NS) & 1, status)) break;
     return;
   }
 
-  // -------------------------------------------------------------- consumers
-  const int nchunks = K / 32;
-  const int bshift = (p.bs == 32) ? 0 : (p.bs == 64 ? 1 : 2);
-  StageIt it = {0, 0};
-  int stage = 0;
-  bool ok = true;
-  for (; it.d < D; ++stage) {
-    const int slot = stage % NS;
-    if (!mbar_wait(&full[slot], (stage / NS) & 1, status)) { ok = false; break; }
-    const SlotHdr h = hdr[slot];
-    const uint8_t* sb = slots + slot * SL.bytes;
-    const float* xs[kTokGroup];
+  // ================================================================ consumers
+  // gate-up / dense: activations resident for the whole kernel (the layer
+  // input is complete before this grid starts: the router, the previous
+  // grid, starts dependents only after its own wait)
+  if (MODE != kModeDown) {
+    // 8 activations per 16-byte load, all loads of a thread issued together
+    const uint4* x8 = static_cast<const uint4*>(p.x16);
+    const int n8 = p.T * K / 8;
+    constexpr int kPer = 4;
+    for (int i0 = tid; i0 < n8; i0 += kCW * 32 * kPer) {
+      uint4 v[kPer];
 #pragma unroll
-    for (int j = 0; j < kTokGroup; ++j) {
-      const int jj = j < h.ntok ? j : 0;
-      if (MODE == kModeDown)
-        xs[j] = reinterpret_cast<const float*>(sb + SL.act) + (size_t)jj * p.src_row_floats;
-      else
-        xs[j] = res + (size_t)h.t[jj] * kdec;
-    }
-    // rows of this stage: gate-up rotates the warp order per stage so all
-    // warps stay busy; down keeps row ownership fixed (deterministic sums).
-    const int first = (MODE == kModeGateUp) ? ((warp - (stage * nrows) % kCW) % kCW + kCW) % kCW : warp;
-    for (int r = first; r < nrows; r += kCW) {
-      float acc0[kTokGroup] = {0.f, 0.f, 0.f, 0.f};
-      row_dot<TS, HAS_ZP>(sb + SL.w[0] + (size_t)r * (K / 2),
-                          reinterpret_cast<const uint16_t*>(sb + SL.s[0] + h.ph[0]) + (size_t)r * nb,
-                          sb + SL.z[0] + h.ph[2] + (size_t)r * nb, nchunks, bshift, xs, h.ntok, acc0, lane);
-      if (MODE == kModeGateUp) {
-        float acc1[kTokGroup] = {0.f, 0.f, 0.f, 0.f};
-        row_dot<TS, HAS_ZP>(sb + SL.w[1] + (size_t)r * (K / 2),
-                            reinterpret_cast<const uint16_t*>(sb + SL.s[1] + h.ph[1]) + (size_t)r * nb,
-                            sb + SL.z[1] + h.ph[3] + (size_t)r * nb, nchunks, bshift, xs, h.ntok, acc1, lane);
-        const int i = r0 + r;
-        const int di = dec_index(i);
-        const float pre = dec_prescale(i);
+      for (int u = 0; u < kPer; ++u) {
+        const int i = i0 + u * kCW * 32;
+        if (i < n8) v[u] = __ldg(x8 + i);
+      }
 #pragma unroll
-        for (int j = 0; j < kTokGroup; ++j) {
-          if (j < h.ntok) {
-            const float g = warp_sum(acc0[j]);
-            const float u = warp_sum(acc1[j]);
-            if (lane == 0) {
-              const float act = g / (1.f + expf(-g)) * u;
-              p.act_out[(size_t)h.a[j] * p.act_row_floats + di] = act * pre;
-            }
-          }
-        }
-      } else if (MODE == kModeDown) {
+      for (int u = 0; u < kPer; ++u) {
+        const int i = i0 + u * kCW * 32;
+        if (i < n8) {
+          const int t = (i * 8) / K, k0 = i * 8 - t * K;
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-        for (int j = 0; j < kTokGroup; ++j) {
-          if (j < h.ntok) {
-            const float y = warp_sum(acc0[j]);
-            if (lane == 0) res[h.t[j] * p.rows_per_cta_max + r] += p.topk_w[h.a[j]] * y;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < kTokGroup; ++j) {
-          if (j < h.ntok) {
-            const float y = warp_sum(acc0[j]);
-            if (lane == 0)
-              static_cast<uint16_t*>(p.out)[(size_t)h.t[j] * N + r0 + r] = Half<TA>::from_float(y);
+          for (int e = 0; e < 8; ++e) {
+            const int kk = k0 + e;
+            const uint16_t b = (uint16_t)(w[e >> 1] >> ((e & 1) * 16));
+            res[t * kdec + dec_index(kk)] = Half<TA>::to_float(b) * dec_prescale(kk);
           }
         }
       }
     }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
+  if (!mbar_wait(route_bar, 0, status)) return;
+  const int nst = *s_nst;
+
+  const uint32_t magic = opaque(0x4B000000u);      // 2^23
+  const uint32_t neg_magic = opaque(0xCB000000u);  // -2^23
+  const ZConst zfixed = zconst(8u, neg_magic);     // no zero-point tensor: zp = 8
+  const int bshift = (p.bs == 32) ? 0 : (p.bs == 64 ? 1 : 2);
+  bool ok = true;
+  int item_base = 0;
+  for (int s = 0; s < nst; ++s) {
+    const int slot = s % NS;
+    // every warp waits for every stage in order (a waiter must never be two
+    // phases ahead of an mbarrier)
+    if (!mbar_wait(&full[slot], (s / NS) & 1, status)) { ok = false; break; }
+    const StageEnt st = s_stage[s];
+    const uint8_t* sb = slots + slot * SL.bytes;
+    // items: for each token group tg (nt tokens), row groups of rows_per_item(nt)
+    constexpr int NMAT = (MODE == kModeGateUp) ? 2 : 1;
+    const int ntg = (st.ntok + kTokGroup - 1) / kTokGroup;
+    int nitems = 0;
+    for (int tg = 0; tg < ntg; ++tg) {
+      const int rg = rows_per_item(min(kTokGroup, st.ntok - tg * kTokGroup), NMAT);
+      nitems += (st.nrows + rg - 1) / rg;
+    }
+    for (int i = ((warp - item_base) % kCW + kCW) % kCW; i < nitems; i += kCW) {
+      int tg = 0, g = i, nt = 0;
+      for (;; ++tg) {
+        nt = min(kTokGroup, st.ntok - tg * kTokGroup);
+        const int ngr = (st.nrows + rows_per_item(nt, NMAT) - 1) / rows_per_item(nt, NMAT);
+        if (g < ngr) break;
+        g -= ngr;
+      }
+      switch (nt) {
+        case 1: run_item<MODE, 1, TS, TA, HAS_ZP>(p, sb, SL, st, s, g, tg, s_perm, res, res, kdec, bshift, magic, neg_magic, zfixed, lane); break;
+        case 2: run_item<MODE, 2, TS, TA, HAS_ZP>(p, sb, SL, st, s, g, tg, s_perm, res, res, kdec, bshift, magic, neg_magic, zfixed, lane); break;
+        case 3: run_item<MODE, 3, TS, TA, HAS_ZP>(p, sb, SL, st, s, g, tg, s_perm, res, res, kdec, bshift, magic, neg_magic, zfixed, lane); break;
+        default: run_item<MODE, 4, TS, TA, HAS_ZP>(p, sb, SL, st, s, g, tg, s_perm, res, res, kdec, bshift, magic, neg_magic, zfixed, lane); break;
+      }
+    }
+    item_base += nitems;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
-    it.g0 += kTokGroup;
-    if (it.g0 >= n_of(it.d)) { ++it.d; it.g0 = 0; }
   }
   if (MODE == kModeDown) {
+    // weighted sum over the selected experts, in stage order (deterministic)
     asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
     if (!ok) return;
+    const int nrows = r1 - r0;
     uint16_t* out = static_cast<uint16_t*>(p.out);
-    for (int i = tid; i < p.T * nrows; i += kCW * 32) {
-      const int t = i / nrows, r = i - t * nrows;
-      float v = res[t * p.rows_per_cta_max + r];
+    for (int idx = tid; idx < p.T * nrows; idx += kCW * 32) {
+      const int t = idx / nrows, r = idx - t * nrows;
+      float v = 0.f;
+      for (int s = 0; s < nst; ++s) {
+        const StageEnt& st = s_stage[s];
+        for (int j = 0; j < st.ntok; ++j) {
+          const int a = s_perm[st.pbase + j];
+          if (a / p.k == t) v = fmaf(s_wt[a], res[((size_t)s * kTokGroup + j) * nrows + r], v);
+        }
+      }
       const size_t o = (size_t)t * N + r0 + r;
       if (p.accumulate) v += Half<TA>::to_float(out[o]);
       out[o] = Half<TA>::from_float(v);
@@ -409,33 +571,58 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(DecodeParams 
 
 // ------------------------------------------------------------------- host
 
-struct DecodePlan {
-  int grid, rows_max, nslots;
-  uint32_t slot_base, smem;
-};
-
 static bool plan_decode(int mode, int T, int N, int K, int bs, bool has_zp, int k, int E, int sms,
                         DecodePlan* out) {
-  DecodePlan P;
-  P.grid = N < sms ? N : sms;
-  P.rows_max = (N + P.grid - 1) / P.grid;
+  DecodePlan P = {};
   const int nb = K / bs;
   const int act_row = dec_row_floats(K);
-  const SlotLayout SL = slot_layout(mode, P.rows_max, K, nb, has_zp, act_row, T);
-  const uint32_t res = (mode == kModeDown) ? (uint32_t)T * P.rows_max * 4 : (uint32_t)T * act_row * 4;
-  P.slot_base = (kFixedSmem + res + 1023u) & ~1023u;
-  if (P.slot_base + 2 * SL.bytes > kSmemBudget) return false;
-  int ns = (int)((kSmemBudget - P.slot_base) / SL.bytes);
-  // no more slots than stages a CTA can have: sum over experts of
-  // ceil(n_e / kTokGroup) with sum n_e = A, at most min(A, E) experts
   const int A = T * k;
-  const int dmax = A < E ? A : E;
-  const int max_stages = (mode == kModeDense) ? (T + kTokGroup - 1) / kTokGroup
-                                              : dmax + (A - dmax + kTokGroup - 1) / kTokGroup;
-  if (ns > max_stages) ns = max_stages < 2 ? 2 : max_stages;
+  const int dmax = (mode == kModeDense) ? 1 : (A < E ? A : E);
+  // a CTA of the previous grid (gate-up) may still occupy the SM while
+  // down streams its first weights: at small T keep both under one SM
+  const uint32_t cap = (T <= kTokGroup) ? (mode == kModeDown ? 100u << 10 : 124u << 10) : kSmemBudget;
+  if (mode == kModeDown) {
+    P.grid = N < sms ? N : sms;
+    P.rows_cta = (N + P.grid - 1) / P.grid;
+    P.slot_rows = P.rows_cta;
+    P.max_stages = dmax + (A - dmax + kTokGroup - 1) / kTokGroup;
+  } else {
+    P.grid = sms;
+    const long long F = (long long)dmax * N;
+    P.rows_cta = (int)((F + P.grid - 1) / P.grid);
+    if (P.rows_cta < 1) P.rows_cta = 1;
+  }
+  P.res_off = kFixedSmem;
+  uint32_t res = 0;
+  if (mode == kModeDown) res = (uint32_t)P.max_stages * kTokGroup * P.rows_cta * 4;
+  else res = (uint32_t)T * act_row * 4;
+  if (mode != kModeDown) {
+    // rows per slot: the CTA's range in as few stages as fit three slots
+    const uint32_t per_row = slot_layout(mode, 1, K, nb, has_zp, act_row, T).bytes;
+    const uint32_t fixed = kFixedSmem + al16(res) + 48 * 64 + 1024;
+    if (fixed + 2 * per_row > cap) return false;
+    int rcap = (int)((cap - fixed) / 3 / (per_row + 16));
+    if (rcap > 64) rcap = 64;
+    if (rcap < 1) rcap = 1;
+    const int nst_min = (P.rows_cta + rcap - 1) / rcap;
+    P.slot_rows = (P.rows_cta + nst_min - 1) / nst_min;
+    if (P.slot_rows > N) P.slot_rows = N;
+    // expert boundaries inside a CTA's range add at most one stage each
+    P.max_stages = nst_min + (P.rows_cta + N - 1) / N + 1;
+    if (mode == kModeDense) P.max_stages = nst_min + 1;
+  }
+  const SlotLayout SL = slot_layout(mode, P.slot_rows, K, nb, has_zp, act_row, T);
+  P.stage_off = P.res_off + al16(res);
+  P.slot_base = (P.stage_off + 48u * P.max_stages + 1023u) & ~1023u;
+  if (P.slot_base + 2 * SL.bytes > kSmemBudget) return false;
+  uint32_t avail = (cap > P.slot_base + 2 * SL.bytes ? cap : P.slot_base + 2 * SL.bytes) - P.slot_base;
+  int ns = (int)(avail / SL.bytes);
+  if (ns > P.max_stages) ns = P.max_stages;
   if (ns > kMaxSlots) ns = kMaxSlots;
+  if (ns < 2) ns = 2;
   P.nslots = ns;
   P.smem = P.slot_base + ns * SL.bytes;
+  if (P.smem > kSmemBudget) return false;
   *out = P;
   return true;
 }
@@ -452,13 +639,10 @@ static cudaError_t launch_decode_t(DecodeParams p, cudaStream_t st, bool pdl) {
   const int E = (MODE == kModeDense) ? 1 : p.E;
   if (!plan_decode(MODE, p.T, p.N, p.K, p.bs, HAS_ZP, p.k, E, device_sm_count(), &P))
     return cudaErrorInvalidValue;
-  p.rows_per_cta_max = P.rows_max;
-  p.nslots = P.nslots;
-  p.slot_base = P.slot_base;
   auto fn = decode_kernel<MODE, TS, TA, HAS_ZP>;
-  cudaError_t err = ensure_smem(decode_kernel<MODE, TS, TA, HAS_ZP>, P.smem);
+  cudaError_t err = ensure_smem(fn, P.smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(fn, dim3(P.grid), dim3(kDecodeThreads), (size_t)P.smem, st, pdl, p);
+  return launch_kernel(fn, dim3(P.grid), dim3(kDecodeThreads), (size_t)P.smem, st, pdl, p, P);
 }
 
 template <int MODE>

@@ -23,29 +23,29 @@ constexpr int kMaxTopk = 8;
 
 // ---- control block (first kCtlBytes of the workspace, zeroed by init)
 constexpr int kCtlStatus = 0;         // u32 sticky status bits
-constexpr int kCtlGroupTicket = 1;    // u32 router: CTAs done with top-k
-constexpr int kCtlTileTicket0 = 16;   // u32[kMaxRouteTiles] router split tickets
-constexpr int kMaxRouteTiles = 64;
+constexpr int kCtlGroupTicket = 1;    // u32 router: token tiles done with top-k
 constexpr size_t kCtlBytes = 1024;
 
 // ---- router tiling
 constexpr int kRouteTokens = 8;       // tokens per router CTA (one warp each)
 constexpr int kRouteThreads = 256;
-constexpr int kMaxSplit = 16;         // H-splits for small T
+constexpr int kMaxSplit = 8;          // H-splits (one cluster) for small T
 
 // ---- decode path
 constexpr int kDecodeMaxTokens = 16;  // T at or below: GEMV path
 constexpr int kTokGroup = 4;          // tokens per decode stage
 
-// Decode-path activation layout.  A K-long fp32 row is stored so that lane l
-// of a warp, processing 16-byte weight chunk c = 32*s + l (32 elements), finds
-// its 32 activations as 8 float4 at ((s*8 + f)*32 + l), f = 0..7: consecutive
-// lanes read consecutive float4 (no bank conflicts).  Element i is
-// pre-multiplied by 16^-(i mod 4): the kernels turn nibble j of a 16-bit
-// half-word into (q - zp) * 16^j exactly, and this power of two undoes it.
-QMOE_HD int dec_row_floats(int K) { return ((K + 1023) / 1024) * 1024; }
+// Decode-path activation layout.  Lane l of a warp processes the two
+// adjacent 16-byte weight chunks c = 64*s + 2*l + u (u = 0, 1; 32 codes
+// each) of a row; the 32 activations of chunk c are 8 float4 at
+// ((s*2 + u)*8 + f)*32 + l, f = 0..7, so consecutive lanes read consecutive
+// float4 (no bank conflicts).  Element i is pre-multiplied by 16^-(i mod 4):
+// the kernels turn nibble j of a 16-bit half-word into (q - zp) * 16^j
+// exactly, and this power of two undoes it.
+QMOE_HD int dec_row_floats(int K) { return ((K + 2047) / 2048) * 2048; }
 QMOE_HD int dec_index(int i) {
-  return ((((i >> 10) * 8 + ((i & 31) >> 2)) * 32 + ((i >> 5) & 31)) << 2) + (i & 3);
+  const int c = i >> 5;
+  return (((((c >> 6) * 2 + (c & 1)) * 8 + ((i & 31) >> 2)) * 32 + ((c & 63) >> 1)) << 2) + (i & 3);
 }
 QMOE_HD float dec_prescale(int i) {
   const int j = i & 3;
@@ -54,22 +54,22 @@ QMOE_HD float dec_prescale(int i) {
 
 // ---- workspace map (byte offsets, each region 256-byte aligned)
 struct WsLayout {
-  size_t ctl, ids, w, offsets, active, perm, partial, act, xp, act16, outacc, tiles, total;
+  size_t ctl, ids, w, offsets, active, perm, act, xp, act16, outacc, tiles, total;
 };
 
 QMOE_HD size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// H-splits per token tile: a cluster of up to 8 CTAs while there are few
+// tiles (T <= 32), one CTA per tile beyond.
 QMOE_HD int route_split(int T) {
   const int tiles = (T + kRouteTokens - 1) / kRouteTokens;
-  if (tiles > 8) return 1;
-  int s = kMaxSplit / tiles;
-  return s < 1 ? 1 : s;
+  if (tiles > 4) return 1;
+  return kMaxSplit / (tiles > 2 ? 4 : tiles);
 }
 
 QMOE_HD WsLayout ws_layout(int T, int H, int I, int E, int k) {
   WsLayout L;
   const size_t A = (size_t)T * k;
-  const int tiles = (T + kRouteTokens - 1) / kRouteTokens;
   size_t o = 0;
   L.ctl = o;      o = align256(o + kCtlBytes);
   L.ids = o;      o = align256(o + A * 4);
@@ -77,8 +77,6 @@ QMOE_HD WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.offsets = o;  o = align256(o + (size_t)(E + 1) * 4);
   L.active = o;   o = align256(o + (size_t)(E + 2) * 4);  // [0] = count, [1..] = ids
   L.perm = o;     o = align256(o + A * 4);
-  L.partial = o;
-  if (route_split(T) > 1) o = align256(o + (size_t)route_split(T) * tiles * kRouteTokens * E * 4);
   L.act = o;  // decode path: act rows in decode layout
   if (T <= kDecodeMaxTokens) o = align256(o + A * dec_row_floats(I) * 4);
   L.xp = o;       o = align256(o + A * (size_t)H * 2);
@@ -104,7 +102,6 @@ struct RouteParams {
   int32_t* active;        // [E+2] workspace: count, ids...
   int32_t* perm;          // [T*k] workspace
   int32_t* user_perm;
-  float* partial;         // [split][tiles*8][E] when split > 1
   uint32_t* ctl;          // control block
 };
 
