@@ -66,8 +66,25 @@ typedef enum {
 
 typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
 
-/* Path selection for qmoe_forward_ex (tests force one path to compare both). */
-typedef enum { QMOE_PATH_AUTO = 0, QMOE_PATH_DECODE = 1, QMOE_PATH_PREFILL = 2 } qmoe_path;
+/* Path selection for qmoe_forward_ex.
+ *   DECODE        per-token GEMV on CUDA cores, fp32 throughout (small T).
+ *   PREFILL       tokens grouped by expert, grouped GEMM on the tensor cores
+ *                 with fp32 accumulation.  Each dequantised weight enters as
+ *                 the exact sum of two operands of the activation dtype
+ *                 (hi = RN(w), lo = w - hi), and the SwiGLU output likewise,
+ *                 so the only roundings are fp32 accumulation, the 16+16-bit
+ *                 SwiGLU output and the final output.
+ *   PREFILL_FAST  the same GEMM with single operands: weights and SwiGLU
+ *                 output rounded once to the activation dtype (bf16/fp16),
+ *                 about half the tensor-core work; relative error of order
+ *                 2^-9 (bf16) of the magnitude of the summed terms.
+ *   AUTO          DECODE for T <= QMOE_DECODE_MAX_TOKENS, else PREFILL. */
+typedef enum {
+  QMOE_PATH_AUTO = 0,
+  QMOE_PATH_DECODE = 1,
+  QMOE_PATH_PREFILL = 2,
+  QMOE_PATH_PREFILL_FAST = 3
+} qmoe_path;
 
 /* One projection for all E experts (see "Packed weights" above). */
 typedef struct {

@@ -196,16 +196,21 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
       (rc = check_qweight(down, H, I, block_size)))
     return rc;
   if ((gate.zp == nullptr) != (up.zp == nullptr)) return QMOE_ERR_INVALID_ARG;
-  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_PREFILL) return QMOE_ERR_INVALID_ARG;
+  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_PREFILL_FAST) return QMOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(T, H, I, E, k);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
   if ((rc = check_device())) return rc;
   const bool zgu = gate.zp != nullptr, zd = down.zp != nullptr;
   const bool dec_ok = T <= kDecodeMaxTokens && decode_fits(kModeGateUp, T, I, H, block_size, zgu, k) &&
                       decode_fits(kModeDown, T, H, I, block_size, zd, k);
+  // the grouped GEMM copies whole rows of scales / zero points in bulk: 16-byte aligned bases
+  const bool split = path != QMOE_PATH_PREFILL_FAST;
+  const bool pre_ok = prefill_fits(H, I, block_size, zgu, zd, split) && aligned(gate.scales, 16) &&
+                      aligned(up.scales, 16) && aligned(down.scales, 16) && aligned(gate.zp, 16) &&
+                      aligned(up.zp, 16) && aligned(down.zp, 16);
   if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
   if (path == QMOE_PATH_DECODE && !dec_ok) return QMOE_ERR_UNSUPPORTED;
-  if (path == QMOE_PATH_PREFILL) return QMOE_ERR_UNSUPPORTED;  // grouped GEMM path not built yet
+  if ((path == QMOE_PATH_PREFILL || path == QMOE_PATH_PREFILL_FAST) && !pre_ok) return QMOE_ERR_UNSUPPORTED;
 
   Ws ws{L, static_cast<uint8_t*>(workspace)};
   cudaStream_t st = (cudaStream_t)stream;
@@ -223,6 +228,37 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   rc = enqueue_route(ws, x, router_w, act_dtype, router_bias, T, H, E, k, topk_w_out, topk_ids_out,
                      nullptr, nullptr, st, pdl);
   if (rc || (rc = mark())) return rc;
+
+  if (path == QMOE_PATH_PREFILL || path == QMOE_PATH_PREFILL_FAST) {
+    PrefillParams p = {};
+    const qmoe_qweight* q[3] = {&gate, &up, &down};
+    for (int m = 0; m < 3; ++m) {
+      p.w[m] = q[m]->w;
+      p.s[m] = q[m]->scales;
+      p.z[m] = q[m]->zp;
+    }
+    p.T = T; p.H = H; p.I = I; p.E = E; p.k = k; p.bs = block_size;
+    p.lbs = block_size == 32 ? 5 : (block_size == 64 ? 6 : 7);
+    p.offsets = ws.at<int32_t>(L.offsets);
+    p.perm = ws.at<int32_t>(L.perm);
+    p.topk_w = ws.at<float>(L.w);
+    p.xp = ws.at<uint16_t>(L.xp);
+    p.act = ws.at<uint16_t>(L.act16);
+    p.act_lo = ws.at<uint16_t>(L.act16lo);
+    p.out_acc = ws.at<float>(L.outacc);
+    p.tiles = ws.at<int32_t>(L.tiles);
+    p.ctl = ws.at<uint32_t>(L.ctl);
+    p.accumulate = accumulate;
+    rc = cuda_status(launch_prefill_permute(p, x, act_dtype, st, pdl));
+    if (rc || (rc = mark())) return rc;
+    rc = cuda_status(launch_prefill_gemm(p, 0, act_dtype, scale_dtype, split, st, pdl));
+    if (rc || (rc = mark())) return rc;
+    rc = cuda_status(launch_prefill_gemm(p, 1, act_dtype, scale_dtype, split, st, pdl));
+    if (rc || (rc = mark())) return rc;
+    rc = cuda_status(launch_prefill_convert(p, out, act_dtype, st, pdl));
+    if (rc) return rc;
+    return mark();
+  }
 
   DecodeParams g = {};
   g.w[0] = gate.w; g.s[0] = gate.scales; g.z[0] = gate.zp;

@@ -43,6 +43,17 @@ cudaError_t launch_decode(DecodeParams p, int mode, int act_dtype, int scale_dty
                           cudaStream_t st, bool pdl);
 bool decode_fits(int mode, int T, int N, int K, int bs, bool has_zp, int k);
 
+// prefill path: token gather + tile table, the two grouped GEMMs (mode 0
+// gate-up with SwiGLU, mode 1 down with the weighted scatter-add), and the
+// final fp32 -> act_dtype conversion (plus residual)
+bool prefill_fits(int H, int I, int bs, bool has_zp_gu, bool has_zp_d, bool split);
+cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int act_dtype, cudaStream_t st,
+                                   bool pdl);
+cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype, int scale_dtype, bool split,
+                                cudaStream_t st, bool pdl);
+cudaError_t launch_prefill_convert(const PrefillParams& p, void* out, int act_dtype, cudaStream_t st,
+                                   bool pdl);
+
 cudaError_t launch_dequant(const uint8_t* w, const void* s, int scale_dtype, const uint8_t* zp,
                            int N, int K, int bs, float* out, cudaStream_t st);
 cudaError_t launch_rmsnorm(const void* x, void* out, int act_dtype, int T, int H, float eps,

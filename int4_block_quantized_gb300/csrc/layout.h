@@ -24,6 +24,7 @@ constexpr int kMaxTopk = 8;
 // ---- control block (first kCtlBytes of the workspace, zeroed by init)
 constexpr int kCtlStatus = 0;         // u32 sticky status bits
 constexpr int kCtlGroupTicket = 1;    // u32 router: token tiles done with top-k
+constexpr int kCtlNtiles = 2;         // u32 prefill: number of token tiles
 constexpr size_t kCtlBytes = 1024;
 
 // ---- router tiling
@@ -54,7 +55,7 @@ QMOE_HD float dec_prescale(int i) {
 
 // ---- workspace map (byte offsets, each region 256-byte aligned)
 struct WsLayout {
-  size_t ctl, ids, w, offsets, active, perm, act, xp, act16, outacc, tiles, total;
+  size_t ctl, ids, w, offsets, active, perm, act, xp, act16, act16lo, outacc, tiles, total;
 };
 
 QMOE_HD size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -81,6 +82,7 @@ QMOE_HD WsLayout ws_layout(int T, int H, int I, int E, int k) {
   if (T <= kDecodeMaxTokens) o = align256(o + A * dec_row_floats(I) * 4);
   L.xp = o;       o = align256(o + A * (size_t)H * 2);
   L.act16 = o;    o = align256(o + A * (size_t)I * 2);
+  L.act16lo = o;  o = align256(o + A * (size_t)I * 2);
   L.outacc = o;   o = align256(o + (size_t)T * H * 4);
   L.tiles = o;    o = align256(o + ((size_t)E + A + 1) * 16);
   L.total = o;
@@ -135,6 +137,26 @@ struct DecodeParams {
   uint32_t slot_base;  // byte offset of the stage ring in shared memory
   int nslots;
   uint32_t* ctl;
+};
+
+// Prefill path (grouped GEMM on the tensor cores).  The token tile table
+// holds 4 ints per tile: expert, first sorted assignment, assignments.
+struct PrefillParams {
+  const uint8_t* w[3];      // gate, up, down packed codes [E, N, K/2]
+  const void* s[3];         // block scales [E, N, K/bs]
+  const uint8_t* z[3];      // zero points [E, N, K/bs] or null
+  int T, H, I, E, k, bs, lbs;  // lbs = log2(bs)
+  const int32_t* offsets;   // [E+1] workspace
+  const int32_t* perm;      // [T*k] workspace: sorted -> assignment t*k+j
+  const float* topk_w;      // [T*k] workspace
+  uint16_t* xp;             // [T*k, H] gathered, K-permuted tokens
+  uint16_t* act;            // [T*k, I] SwiGLU output (high part), K-permuted
+  uint16_t* act_lo;         // [T*k, I] SwiGLU output minus its high part (split path)
+  float* out_acc;           // [T, H] fp32 accumulator
+  int32_t* tiles;           // [ntiles][4]
+  uint32_t* ctl;            // control block (status, tile count)
+  int accumulate;
+  int nst, nsz;             // pipeline stages, tile scale buffers (set per GEMM launch)
 };
 
 }  // namespace qmoe

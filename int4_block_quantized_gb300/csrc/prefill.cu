@@ -1,0 +1,690 @@
+// prefill.cu -- large-T path of the layer: tokens grouped by expert, then a
+// grouped expert GEMM on the 5th-generation tensor cores (tcgen05) with the
+// int4 weights dequantised on chip, SwiGLU fused into the gate-up epilogue
+// and the routing-weighted scatter-add fused into the down epilogue.
+//
+// Sources: "Qwen MoE BringUp" (IREE ONNX Runtime EP issue #34), IR guide
+// "Optimization Opportunities" item 9 (sort tokens by expert, one grouped
+// GEMM over all experts using the grouping as a gather index, weighted
+// un-permute) and item 6 (DequantizeLinear fused into the MatMul);
+// DequantizeLinear with block_size from local fix A1; SwiGLU and the
+// weighted sum from IR guide 3, Expert Computation steps 5-7.
+//
+// GB300 design.  Swap-AB: the weight rows are the MMA's M = 128 operand and
+// an expert's tokens (up to 128 per tile) its N, so small experts still fill
+// the tensor core's M dimension.  A gate-up tile stacks 64 gate rows over
+// the same 64 up rows, so gate and up land in one TMEM accumulator and the
+// SwiGLU pairs them in the epilogue.  Per CTA (one per SM, persistent):
+//   warp 0  TMA producer: packed int4 tile (128 rows x 64 codes) + the
+//           tile's block scales / zero points + the token tile (bf16/fp16,
+//           128-byte swizzle) into a 4-stage ring;
+//   warp 1  TMEM allocation and the single-thread tcgen05.mma issuer;
+//   warps 2-5  dequantisers: one thread per weight row turns 64 codes into
+//           RN_operand((q - zp) * scale) and writes them in the canonical
+//           128-byte-swizzled K-major layout the MMA descriptor reads;
+//   warps 6-9  epilogue: tcgen05.ld of the accumulator (double-buffered in
+//           TMEM so the next tile's MMAs overlap), SwiGLU or the weighted
+//           fp32 scatter-add.
+// The dequantised values are exact integers times the scale, rounded once to
+// the operand type; K is permuted inside every group of 8 (order 0,4,1,5,
+// 2,6,3,7) identically for weights and activations so one LOP3 yields two
+// operands from a 32-bit word of codes.
+#include <cuda.h>
+#include <math.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace qmoe {
+
+constexpr int kGemmThreads = 320;  // 10 warps
+constexpr int kStages = 4;
+constexpr int kBN = 128;           // max tokens per tile (TMEM columns per accumulator)
+constexpr int kBoxRows = 32;       // token rows per B TMA box
+constexpr int kModeGU = 0, kModeDN = 1;
+
+// position of element j (0..7) of a group of 8 in the permuted K order
+__host__ __device__ __forceinline__ int kperm_pos(int j) { return (j & 3) * 2 + (j >> 2); }
+
+
+// ---------------------------------------------------------------- permute
+// xp[r] = x[token of sorted assignment r] with K permuted inside each group
+// of 8; out_acc = 0; block 0 also writes the token tile table: an expert
+// with n assignments gets ceil(n/128) tiles of balanced size.
+__global__ void __launch_bounds__(256) permute_kernel(const uint16_t* __restrict__ x, PrefillParams p) {
+  pdl_wait();
+  const int H = p.H, A = p.T * p.k;
+  if (blockIdx.x == 0) {
+    __shared__ int s_scan[kMaxExperts];
+    const int e = threadIdx.x;
+    int n = 0, tl = 0;
+    if (e < p.E) {
+      n = __ldcg(p.offsets + e + 1) - __ldcg(p.offsets + e);
+      tl = (n + kBN - 1) / kBN;
+    }
+    s_scan[e] = tl;
+    __syncthreads();
+    for (int o = 1; o < kMaxExperts; o <<= 1) {  // inclusive scan
+      const int v = e >= o ? s_scan[e - o] : 0;
+      __syncthreads();
+      s_scan[e] += v;
+      __syncthreads();
+    }
+    if (tl > 0) {
+      const int base = s_scan[e] - tl;
+      const int rows = (n + tl - 1) / tl;
+      const int off = __ldcg(p.offsets + e);
+      for (int i = 0; i < tl; ++i) {
+        int32_t* d = p.tiles + 4 * (base + i);
+        d[0] = e;
+        d[1] = off + i * rows;
+        d[2] = min(rows, n - i * rows);
+        d[3] = 0;
+      }
+    }
+    if (e == kMaxExperts - 1) p.ctl[kCtlNtiles] = (uint32_t)s_scan[e];
+  }
+  const int groups = H / 8;  // 16 bytes = one group of 8 per step
+  for (int r = blockIdx.x; r < A; r += gridDim.x) {
+    const int t = __ldcg(p.perm + r) / p.k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(p.xp + (size_t)r * H);
+    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+      const uint4 v = __ldg(src + g);
+      uint4 o;  // (e0,e1,..,e7) -> (e0,e4,e1,e5,e2,e6,e3,e7)
+      o.x = __byte_perm(v.x, v.z, 0x5410);
+      o.y = __byte_perm(v.x, v.z, 0x7632);
+      o.z = __byte_perm(v.y, v.w, 0x5410);
+      o.w = __byte_perm(v.y, v.w, 0x7632);
+      dst[g] = o;
+    }
+  }
+  const size_t n4 = (size_t)p.T * H / 4;
+  float4* acc = reinterpret_cast<float4*>(p.out_acc);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  pdl_trigger();
+}
+
+// ---------------------------------------------------------------- convert
+// out = act_dtype(out_acc (+ out if accumulating)), 4 elements per step
+template <typename TA>
+__global__ void __launch_bounds__(256) convert_kernel(PrefillParams p, uint16_t* __restrict__ out) {
+  pdl_wait();
+  const size_t n4 = (size_t)p.T * p.H / 4;
+  const float4* acc = reinterpret_cast<const float4*>(p.out_acc);
+  uint2* o = reinterpret_cast<uint2*>(out);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    float4 v = __ldcg(acc + i);
+    if (p.accumulate) {
+      const uint2 r = o[i];
+      v.x += Half<TA>::to_float((uint16_t)(r.x & 0xFFFFu));
+      v.y += Half<TA>::to_float((uint16_t)(r.x >> 16));
+      v.z += Half<TA>::to_float((uint16_t)(r.y & 0xFFFFu));
+      v.w += Half<TA>::to_float((uint16_t)(r.y >> 16));
+    }
+    uint2 w;
+    w.x = (uint32_t)Half<TA>::from_float(v.x) | ((uint32_t)Half<TA>::from_float(v.y) << 16);
+    w.y = (uint32_t)Half<TA>::from_float(v.z) | ((uint32_t)Half<TA>::from_float(v.w) << 16);
+    o[i] = w;
+  }
+}
+
+// ------------------------------------------------------------ dequant core
+// Two codes (the 4-bit fields at bits [0,4) and [16,20) of v) of one scale
+// block to packed operand pairs.  w = (q - zp) * s is exact in fp32 (at most
+// 4 + 11 significant bits); hi = RN_OT(w) and lo = w - hi, which OT holds
+// exactly (the remainder has at most 7 significant bits), so hi + lo == w.
+// "Magic" constants: 0x4300 | q is the bf16 number 128 + q and 0x6400 | q
+// the fp16 number 1024 + q, so (magic | q) - (magic | zp) = q - zp exactly.
+template <uint32_t MAGIC>
+__device__ __forceinline__ uint32_t magic_pair(uint32_t v) {
+  uint32_t h;
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(h) : "r"(v), "n"(MAGIC));
+  return h;
+}
+__device__ __forceinline__ uint32_t u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ uint32_t u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __nv_bfloat162 bf2(uint32_t v) { return *reinterpret_cast<__nv_bfloat162*>(&v); }
+__device__ __forceinline__ __half2 h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
+template <typename OT, typename TS>
+struct Deq;
+// bf16 operands, bf16 scales: qz * s has <= 12 significant bits
+template <>
+struct Deq<__nv_bfloat16, __nv_bfloat16> {
+  __nv_bfloat162 zc, sc;
+  __device__ __forceinline__ void set(uint32_t zp, uint16_t s) {
+    zc = __bfloat162bfloat162(__ushort_as_bfloat16((uint16_t)(0x4300u | zp)));
+    sc = __bfloat162bfloat162(__ushort_as_bfloat16(s));
+  }
+  __device__ __forceinline__ uint32_t hi(uint32_t v) const {
+    return u32(__hmul2(__hsub2(bf2(magic_pair<0x43004300u>(v)), zc), sc));
+  }
+  __device__ __forceinline__ void both(uint32_t v, uint32_t& h, uint32_t& l) const {
+    const __nv_bfloat162 qz = __hsub2(bf2(magic_pair<0x43004300u>(v)), zc);
+    const __nv_bfloat162 hv = __hmul2(qz, sc);
+    h = u32(hv);
+    l = u32(__hfma2(qz, sc, __hneg2(hv)));
+  }
+};
+// bf16 operands, fp16 scales: s = sh + sl with sh = RN_bf16(s) and sl exact
+// (<= 3 bits); c = qz * sl is exact, hi = RN(qz * sh + c) = RN(w),
+// d = qz * sh - hi and lo = d + c = w - hi are exact.
+template <>
+struct Deq<__nv_bfloat16, __half> {
+  __nv_bfloat162 zc, shc, slc;
+  __device__ __forceinline__ void set(uint32_t zp, uint16_t s) {
+    zc = __bfloat162bfloat162(__ushort_as_bfloat16((uint16_t)(0x4300u | zp)));
+    const float sf = __half2float(__ushort_as_half(s));
+    const __nv_bfloat16 sh = __float2bfloat16_rn(sf);
+    shc = __bfloat162bfloat162(sh);
+    slc = __bfloat162bfloat162(__float2bfloat16_rn(sf - __bfloat162float(sh)));
+  }
+  __device__ __forceinline__ uint32_t hi(uint32_t v) const {
+    const __nv_bfloat162 qz = __hsub2(bf2(magic_pair<0x43004300u>(v)), zc);
+    return u32(__hfma2(qz, shc, __hmul2(qz, slc)));
+  }
+  __device__ __forceinline__ void both(uint32_t v, uint32_t& h, uint32_t& l) const {
+    const __nv_bfloat162 qz = __hsub2(bf2(magic_pair<0x43004300u>(v)), zc);
+    const __nv_bfloat162 c = __hmul2(qz, slc);
+    const __nv_bfloat162 hv = __hfma2(qz, shc, c);
+    h = u32(hv);
+    l = u32(__hadd2(__hfma2(qz, shc, __hneg2(hv)), c));
+  }
+};
+// fp16 operands (fp16 scales, or bf16 scales converted exactly to fp16):
+// qz * s has <= 15 significant bits; exact split for scales >= 2^-14
+template <typename TS>
+struct DeqF16 {
+  __half2 zc, sc;
+  __device__ __forceinline__ void set(uint32_t zp, uint16_t s) {
+    zc = __half2half2(__ushort_as_half((uint16_t)(0x6400u | zp)));
+    sc = __half2half2(__float2half_rn(Half<TS>::to_float(s)));
+  }
+  __device__ __forceinline__ uint32_t hi(uint32_t v) const {
+    return u32(__hmul2(__hsub2(h2(magic_pair<0x64006400u>(v)), zc), sc));
+  }
+  __device__ __forceinline__ void both(uint32_t v, uint32_t& h, uint32_t& l) const {
+    const __half2 qz = __hsub2(h2(magic_pair<0x64006400u>(v)), zc);
+    const __half2 hv = __hmul2(qz, sc);
+    h = u32(hv);
+    l = u32(__hfma2(qz, sc, __hneg2(hv)));
+  }
+};
+template <> struct Deq<__half, __half> : DeqF16<__half> {};
+template <> struct Deq<__half, __nv_bfloat16> : DeqF16<__nv_bfloat16> {};
+
+// fp32 -> (hi, lo) operand pair of the activation (split path)
+template <typename OT>
+__device__ __forceinline__ void split_act(float a, uint16_t& h, uint16_t& l) {
+  h = Half<OT>::from_float(a);
+  l = Half<OT>::from_float(a - Half<OT>::to_float(h));
+}
+
+// ------------------------------------------------------------ grouped GEMM
+constexpr uint32_t kTileOp = 128 * 128;    // 16-bit operand tile: 128 rows x 64 K (SW128)
+constexpr uint32_t kStagePk = 128 * 32;    // packed codes: 128 rows x 64 codes
+constexpr uint32_t kGbufFloats = 64 * 17;  // gate values of one 16-column chunk (padded rows)
+constexpr uint32_t kTmemCols = 256;        // two 128-column accumulators
+constexpr uint32_t kSmemLimit = 232448;    // 227 KB per CTA
+
+// Stage: [A hi][A lo (split)][B hi][B lo (split down)][packed codes]
+struct GemmSmem {
+  uint32_t a_lo, b_hi, b_lo, pk, stage;  // offsets inside a stage, stage size
+  uint32_t sz_bytes, sz_off, stage_off, gbuf_off, total;
+};
+__host__ __device__ inline GemmSmem gemm_smem(int mode, bool split, int nb, bool has_zp, int nst, int nsz) {
+  GemmSmem S;
+  const uint32_t na = split ? 2 : 1, nbt = (split && mode == kModeDN) ? 2 : 1;
+  S.a_lo = kTileOp;
+  S.b_hi = na * kTileOp;
+  S.b_lo = S.b_hi + kTileOp;
+  S.pk = S.b_hi + nbt * kTileOp;
+  S.stage = S.pk + kStagePk;
+  S.sz_bytes = ((uint32_t)128 * nb * 2 + (has_zp ? (uint32_t)128 * nb : 0u) + 1023u) & ~1023u;
+  S.sz_off = 1024;
+  S.stage_off = S.sz_off + nsz * S.sz_bytes;
+  S.gbuf_off = S.stage_off + nst * S.stage;
+  S.total = S.gbuf_off + (mode == kModeGU ? 2 * kGbufFloats * 4 : 0) + 1024;  // + base alignment slack
+  return S;
+}
+// deepest pipeline that fits (4..2 stages); at equal depth two tile-scale buffers
+__host__ inline bool gemm_plan(int mode, bool split, int nb, bool has_zp, int& nst, int& nsz) {
+  for (int st = kStages; st >= 2; --st)
+    for (int sz = 2; sz >= 1; --sz)
+      if (gemm_smem(mode, split, nb, has_zp, st, sz).total <= kSmemLimit) {
+        nst = st;
+        nsz = sz;
+        return true;
+      }
+  return false;
+}
+
+// bounded wait that also gives up once another role has aborted
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                              volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 63u) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        set_status(status, QMOE_ST_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// ring position: slot index and the parity of its current use
+struct Ring {
+  int i = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++i == n) {
+      i = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// One persistent CTA per SM.  Work item t = (weight row block mb, token
+// tile nt), nt fastest, so the token tiles of one expert run side by side
+// and share the weight tile through L2.
+template <int MODE, typename TA, typename TS, bool HAS_ZP, bool SPLIT>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+                const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  constexpr bool GU = MODE == kModeGU;
+  constexpr bool BLO = SPLIT && !GU;  // second B tile (activation low part)
+  const int K = GU ? p.H : p.I;       // reduction length
+  const int NR = GU ? p.I : p.H;      // weight rows per expert matrix
+  const int nb = K >> p.lbs;
+  const int nst = p.nst, nsz = p.nsz;
+  const GemmSmem L = gemm_smem(MODE, SPLIT, nb, HAS_ZP, nst, nsz);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* tma_full = bars;                // [kStages] packed codes + tokens landed
+  uint64_t* a_full = bars + kStages;        // [kStages] operand dequantised
+  uint64_t* empty = bars + 2 * kStages;     // [kStages] MMAs done with the stage
+  uint64_t* tmem_full = bars + 3 * kStages; // [2] accumulator complete
+  uint64_t* tmem_empty = tmem_full + 2;     // [2] accumulator drained
+  uint64_t* sz_full = tmem_empty + 2;       // [2] tile scales landed
+  uint64_t* sz_empty = sz_full + 2;         // [2] tile scales no longer read
+  uint64_t* gx_full = sz_empty + 2;         // [2] gate chunk in the exchange buffer
+  uint64_t* gx_empty = gx_full + 2;         // [2] exchange buffer free
+  uint64_t* fin = gx_empty + 2;             // drain on abort
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(fin + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint8_t* szbuf = smem + L.sz_off;
+  uint8_t* stages = smem + L.stage_off;
+  float* gbuf = reinterpret_cast<float*>(smem + L.gbuf_off);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t* status = p.ctl + kCtlStatus;
+  const int KC = K / 64;
+  const int MB = NR / (GU ? 64 : 128);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&tma_full[s], 1);
+      mbar_init(&a_full[s], 128);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 128);
+      mbar_init(&sz_full[b], 1);
+      mbar_init(&sz_empty[b], 128);
+      mbar_init(&gx_full[b], 64);
+      mbar_init(&gx_empty[b], 64);
+    }
+    mbar_init(fin, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  pdl_wait();  // routing, token tiles and (down) the SwiGLU output come from earlier grids
+  pdl_trigger();
+  const int NT = (int)__ldcg(p.ctl + kCtlNtiles);
+  const int ntile_total = NT * MB;
+  const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
+
+  if (warp == 0) {
+    // ============================================================ producer
+    if (lane == 0) {
+      int it = 0, tc = 0;
+      Ring rs, rz;
+      const uint32_t sbytes = 128u * nb * 2, zbytes = HAS_ZP ? 128u * nb : 0u;
+      for (int t = blockIdx.x; t < ntile_total && !*s_abort; t += gridDim.x, ++tc, rz.next(nsz)) {
+        const int4 tl = __ldcg(tiles + t % NT);
+        const int mb = t / NT;
+        const int e = tl.x, row0 = tl.y, npad = (tl.z + 15) & ~15;
+        const int nbox = (npad + kBoxRows - 1) / kBoxRows;
+        if (tc >= nsz && !wait_or_abort(&sz_empty[rz.i], rz.ph ^ 1u, status, s_abort)) break;
+        // block scales / zero points of the tile's 128 weight rows over the whole K
+        uint8_t* sz = szbuf + rz.i * L.sz_bytes;
+        uint64_t* zb = &sz_full[rz.i];
+        mbar_arrive_expect_tx(zb, sbytes + zbytes);
+        if (GU) {
+          const size_t r = (size_t)e * NR + mb * 64;
+          bulk_g2s(sz, static_cast<const uint8_t*>(p.s[0]) + r * nb * 2, sbytes / 2, zb);
+          bulk_g2s(sz + sbytes / 2, static_cast<const uint8_t*>(p.s[1]) + r * nb * 2, sbytes / 2, zb);
+          if (HAS_ZP) {
+            bulk_g2s(sz + sbytes, p.z[0] + r * nb, zbytes / 2, zb);
+            bulk_g2s(sz + sbytes + zbytes / 2, p.z[1] + r * nb, zbytes / 2, zb);
+          }
+        } else {
+          const size_t r = (size_t)e * NR + mb * 128;
+          bulk_g2s(sz, static_cast<const uint8_t*>(p.s[2]) + r * nb * 2, sbytes, zb);
+          if (HAS_ZP) bulk_g2s(sz + sbytes, p.z[2] + r * nb, zbytes, zb);
+        }
+        const uint32_t btx = nbox * kBoxRows * 128 * (BLO ? 2 : 1);
+        for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst)) {
+          if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) break;
+          uint8_t* st = stages + rs.i * L.stage;
+          uint64_t* fb = &tma_full[rs.i];
+          mbar_arrive_expect_tx(fb, kStagePk + btx);
+          if (GU) {
+            tma_load_2d(st + L.pk, &tm_a0, kc * 32, e * NR + mb * 64, fb);
+            tma_load_2d(st + L.pk + 64 * 32, &tm_a1, kc * 32, e * NR + mb * 64, fb);
+          } else {
+            tma_load_2d(st + L.pk, &tm_a0, kc * 32, e * NR + mb * 128, fb);
+          }
+          for (int bx = 0; bx < nbox; ++bx) {
+            tma_load_2d(st + L.b_hi + bx * kBoxRows * 128, &tm_b, kc * 64, row0 + bx * kBoxRows, fb);
+            if (BLO) tma_load_2d(st + L.b_lo + bx * kBoxRows * 128, &tm_b2, kc * 64, row0 + bx * kBoxRows, fb);
+          }
+        }
+      }
+      if (*s_abort) {  // let the copies already issued land before the CTA exits
+        for (int s = 0; s < nst; ++s)
+          if (it > s) mbar_wait(&tma_full[s], ((it - 1 - s) / nst) & 1, nullptr);
+        for (int b = 0; b < nsz; ++b)
+          if (tc > b) mbar_wait(&sz_full[b], ((tc - 1 - b) / nsz) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      int tc = 0;
+      bool issued = false;
+      Ring rs;
+      constexpr bool bf = std::is_same<TA, __nv_bfloat16>::value;
+      for (int t = blockIdx.x; t < ntile_total; t += gridDim.x, ++tc) {
+        const int4 tl = __ldcg(tiles + t % NT);
+        const uint32_t idesc = idesc_f16(128, (tl.z + 15) & ~15, bf);
+        const int b = tc & 1;
+        if (tc >= 2 && !wait_or_abort(&tmem_empty[b], ((tc >> 1) - 1) & 1, status, s_abort)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * kBN;
+        bool ok = true;
+        for (int kc = 0; kc < KC; ++kc, rs.next(nst)) {
+          if (!wait_or_abort(&a_full[rs.i], rs.ph, status, s_abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(stages + rs.i * L.stage);
+          const uint64_t ah = sw128_desc(st), al = sw128_desc(st + L.a_lo);
+          const uint64_t bh = sw128_desc(st + L.b_hi), bl = sw128_desc(st + L.b_lo);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // K = 16 per instruction: +32 bytes in the swizzled row
+            mma_f16_ss(d_tmem, ah + 2 * kk, bh + 2 * kk, idesc, (kc | kk) != 0);
+            if (SPLIT) mma_f16_ss(d_tmem, al + 2 * kk, bh + 2 * kk, idesc, 1u);
+            if (BLO) mma_f16_ss(d_tmem, ah + 2 * kk, bl + 2 * kk, idesc, 1u);
+          }
+          issued = true;
+          mma_commit(&empty[rs.i]);
+        }
+        if (!ok) break;
+        mma_commit(&tmem_full[b]);
+      }
+      if (*s_abort && issued) {  // MMAs still in flight must finish before TMEM is freed
+        mma_commit(fin);
+        mbar_wait(fin, 0, nullptr);
+      }
+    }
+  } else if (warp < 6) {
+    // ============================================================ dequantisers
+    const int r = (warp & 3) * 32 + lane;  // weight row of the tile
+    Ring rs, rz;
+    for (int t = blockIdx.x; t < ntile_total; t += gridDim.x, rz.next(nsz)) {
+      if (!wait_or_abort(&sz_full[rz.i], rz.ph, status, s_abort)) break;
+      const uint8_t* sz = szbuf + rz.i * L.sz_bytes;
+      const uint16_t* srow = reinterpret_cast<const uint16_t*>(sz) + (size_t)r * nb;
+      const uint8_t* zrow = sz + 128u * nb * 2 + (size_t)r * nb;
+      bool ok = true;
+      for (int kc = 0; kc < KC; ++kc, rs.next(nst)) {
+        if (!wait_or_abort(&tma_full[rs.i], rs.ph, status, s_abort)) { ok = false; break; }
+        uint8_t* st = stages + rs.i * L.stage;
+        const uint4* pk = reinterpret_cast<const uint4*>(st + L.pk + r * 32);
+        const uint4 q0 = pk[0], q1 = pk[1];
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // block_size >= 32: codes 0-31 of the chunk share one block, 32-63 one block
+        const int blo = (kc * 64) >> p.lbs, bhi = (kc * 64 + 32) >> p.lbs;
+        Deq<TA, TS> dq[2];
+        dq[0].set(HAS_ZP ? (uint32_t)zrow[blo] : 8u, srow[blo]);
+        dq[1].set(HAS_ZP ? (uint32_t)zrow[bhi] : 8u, srow[bhi]);
+        const uint32_t roff = (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const Deq<TA, TS>& d = dq[g >> 2];
+          const uint32_t off = roff + ((g ^ (r & 7)) << 4);  // 128-byte swizzle
+          uint4 h, l;  // elements (0,4), (1,5), (2,6), (3,7) of the group
+          if (SPLIT) {
+            d.both(w[g], h.x, l.x);
+            d.both(w[g] >> 4, h.y, l.y);
+            d.both(w[g] >> 8, h.z, l.z);
+            d.both(w[g] >> 12, h.w, l.w);
+            *reinterpret_cast<uint4*>(st + off) = h;
+            *reinterpret_cast<uint4*>(st + L.a_lo + off) = l;
+          } else {
+            h.x = d.hi(w[g]);
+            h.y = d.hi(w[g] >> 4);
+            h.z = d.hi(w[g] >> 8);
+            h.w = d.hi(w[g] >> 12);
+            *reinterpret_cast<uint4*>(st + off) = h;
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&a_full[rs.i]);
+      }
+      if (!ok) break;
+      mbar_arrive(&sz_empty[rz.i]);
+    }
+  } else {
+    // ============================================================ epilogue
+    const int q = warp & 3;         // TMEM lane quadrant this warp may read
+    const int row = q * 32 + lane;  // accumulator row = weight row of the tile
+    int tc = 0, cc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntile_total; t += gridDim.x, ++tc) {
+      const int4 tl = __ldcg(tiles + t % NT);
+      const int mb = t / NT;
+      const int row0 = tl.y, nrows = tl.z, npad = (nrows + 15) & ~15;
+      const int b = tc & 1;
+      if (!wait_or_abort(&tmem_full[b], (tc >> 1) & 1, status, s_abort)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
+      for (int c0 = 0; c0 < npad; c0 += 16, ++cc) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c0, v);
+        if (GU) {
+          // rows 0-63 gate, 64-127 up of the same 64 intermediate indices
+          const int xb = cc & 1;
+          float* gx = gbuf + xb * kGbufFloats;
+          if (q < 2) {
+            if (cc >= 2 && !wait_or_abort(&gx_empty[xb], ((cc >> 1) - 1) & 1, status, s_abort)) { ok = false; break; }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) gx[row * 17 + j] = __uint_as_float(v[j]);
+            mbar_arrive(&gx_full[xb]);
+          } else {
+            if (!wait_or_abort(&gx_full[xb], (cc >> 1) & 1, status, s_abort)) { ok = false; break; }
+            const int i = row - 64;
+            const int ig = mb * 64 + i;
+            const size_t col = (ig & ~7) + kperm_pos(ig & 7);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < nrows) {
+                const float g = gx[i * 17 + j];
+                const float a = g / (1.f + expf(-g)) * __uint_as_float(v[j]);
+                const size_t o = (size_t)(row0 + c0 + j) * p.I + col;
+                if (SPLIT) {
+                  uint16_t h, l;
+                  split_act<TA>(a, h, l);
+                  p.act[o] = h;
+                  p.act_lo[o] = l;
+                } else {
+                  p.act[o] = Half<TA>::from_float(a);
+                }
+              }
+            }
+            mbar_arrive(&gx_empty[xb]);
+          }
+        } else {
+          const int h = mb * 128 + row;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < nrows) {
+              const int a = __ldg(p.perm + row0 + c0 + j);
+              atomicAdd(p.out_acc + (size_t)(a / p.k) * p.H + h, __ldg(p.topk_w + a) * __uint_as_float(v[j]));
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      tc_fence_before();
+      mbar_arrive(&tmem_empty[b]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda)
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2D map over a row-major [rows, inner] tensor with box {box_inner, box_rows}
+static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt, uint64_t inner,
+                     uint64_t rows, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * elt};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool prefill_fits(int H, int I, int bs, bool has_zp_gu, bool has_zp_d, bool split) {
+  if (H % 128 || I % 64 || bs < 32 || (bs & (bs - 1))) return false;
+  int a, b;
+  return gemm_plan(kModeGU, split, H / bs, has_zp_gu, a, b) && gemm_plan(kModeDN, split, I / bs, has_zp_d, a, b);
+}
+
+cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int, cudaStream_t st, bool pdl) {
+  const int A = p.T * p.k;
+  const int blocks = A < 1024 ? A : 1024;
+  return launch_kernel(permute_kernel, dim3(blocks), dim3(256), 0, st, pdl, static_cast<const uint16_t*>(x), p);
+}
+
+template <int MODE, typename TA, typename TS, bool Z, bool SPLIT>
+static cudaError_t launch_gemm_t(PrefillParams p, const CUtensorMap* m, cudaStream_t st, bool pdl) {
+  const int K = (MODE == kModeGU) ? p.H : p.I;
+  if (!gemm_plan(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz)) return cudaErrorInvalidValue;
+  const GemmSmem L = gemm_smem(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz);
+  auto fn = gemm_kernel<MODE, TA, TS, Z, SPLIT>;
+  cudaError_t err = ensure_smem(fn, L.total);
+  if (err != cudaSuccess) return err;
+  return launch_kernel(fn, dim3(device_sm_count()), dim3(kGemmThreads), (size_t)L.total, st, pdl, m[0], m[1], m[2],
+                       m[3], p);
+}
+
+template <int MODE, typename TA, typename TS>
+static cudaError_t dispatch_zs(const PrefillParams& p, bool z, bool split, const CUtensorMap* m, cudaStream_t st,
+                               bool pdl) {
+  if (split) return z ? launch_gemm_t<MODE, TA, TS, true, true>(p, m, st, pdl)
+                      : launch_gemm_t<MODE, TA, TS, false, true>(p, m, st, pdl);
+  return z ? launch_gemm_t<MODE, TA, TS, true, false>(p, m, st, pdl)
+           : launch_gemm_t<MODE, TA, TS, false, false>(p, m, st, pdl);
+}
+
+template <int MODE>
+static cudaError_t dispatch_gemm(const PrefillParams& p, int act_dtype, int scale_dtype, bool z, bool split,
+                                 const CUtensorMap* m, cudaStream_t st, bool pdl) {
+  if (act_dtype == 1)
+    return scale_dtype == 1 ? dispatch_zs<MODE, __nv_bfloat16, __nv_bfloat16>(p, z, split, m, st, pdl)
+                            : dispatch_zs<MODE, __nv_bfloat16, __half>(p, z, split, m, st, pdl);
+  return scale_dtype == 1 ? dispatch_zs<MODE, __half, __nv_bfloat16>(p, z, split, m, st, pdl)
+                          : dispatch_zs<MODE, __half, __half>(p, z, split, m, st, pdl);
+}
+
+cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype, int scale_dtype, bool split,
+                                cudaStream_t st, bool pdl) {
+  const int A = p.T * p.k;
+  const CUtensorMapDataType adt = act_dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap m[4];
+  if (mode == kModeGU) {
+    if (!make_map(&m[0], p.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.H / 2, (uint64_t)p.E * p.I, 32, 64,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&m[1], p.w[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.H / 2, (uint64_t)p.E * p.I, 32, 64,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&m[2], p.xp, adt, 2, p.H, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorNotSupported;
+    m[3] = m[2];
+    return dispatch_gemm<kModeGU>(p, act_dtype, scale_dtype, p.z[0] != nullptr, split, m, st, pdl);
+  }
+  if (!make_map(&m[0], p.w[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.I / 2, (uint64_t)p.E * p.H, 32, 128,
+                CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&m[2], p.act, adt, 2, p.I, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[3], split ? p.act_lo : p.act, adt, 2, p.I, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorNotSupported;
+  m[1] = m[0];
+  return dispatch_gemm<kModeDN>(p, act_dtype, scale_dtype, p.z[2] != nullptr, split, m, st, pdl);
+}
+
+cudaError_t launch_prefill_convert(const PrefillParams& p, void* out, int act_dtype, cudaStream_t st, bool pdl) {
+  const size_t n4 = (size_t)p.T * p.H / 4;
+  const int blocks = (int)((n4 + 255) / 256 < 2048 ? (n4 + 255) / 256 : 2048);
+  if (act_dtype == 1)
+    return launch_kernel(convert_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, st, pdl, p,
+                         static_cast<uint16_t*>(out));
+  return launch_kernel(convert_kernel<__half>, dim3(blocks), dim3(256), 0, st, pdl, p, static_cast<uint16_t*>(out));
+}
+
+}  // namespace qmoe

@@ -1,0 +1,163 @@
+"""GPU parity of the prefill path (tokens grouped by expert, grouped GEMM on
+the tensor cores with on-chip dequantisation) against the fp64 oracle.
+
+Small shapes are compared on every token; the full-size workloads on a
+seeded sample of tokens (each token's output depends only on that token, so
+the oracle runs on the sampled rows alone).  The default prefill path (exact
+hi + lo operands) meets the decode path's bar: ids exact outside near ties,
+output within 1e-2 * (1 + |ref|) elementwise.  The single-operand fast path
+rounds weights and SwiGLU output to bf16/fp16; it is held to the elementwise
+bar on small-magnitude cases and, at the full-size magnitudes, to the same
+bound taken over the whole output: max|err| <= 1e-2 * (1 + max|ref|)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int4_block_quantized_gb300 import binding as B
+from int4_block_quantized_gb300 import synthetic as S
+from qmoe_check import assert_close_layer, check_routing
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int4_block_quantized_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def check_prefill(wl, L=None, seed=0, sample=None, accumulate=False, path=B.PATH_PREFILL, normwise=False):
+    L = L or S.make_layer(wl, seed=seed, device=DEV)
+    x = L["x"]
+    T = x.shape[0]
+    out = out0 = None
+    if accumulate:
+        out0 = torch.randn(x.shape, generator=torch.Generator(device=DEV).manual_seed(seed + 7),
+                           device=DEV).to(x.dtype)
+        out = out0.clone()
+    ws = B.Workspace(T, wl.H, wl.I, wl.E, wl.k)
+    o, tw, ti = B.qmoe_forward(L, out=out, ws=ws, accumulate=accumulate, path=path, return_routing=True)
+    torch.cuda.synchronize()
+    rc, bits = ws.status()
+    assert rc == 0 and bits == 0
+    if sample is None:
+        idx = np.arange(T)
+    else:
+        idx = np.sort(np.random.default_rng(seed + 11).choice(T, size=min(sample, T), replace=False))
+    tidx = torch.as_tensor(idx, device=DEV)
+    Ls = dict(L, x=x[tidx].contiguous(), T=len(idx))
+    ref, ref_ids, ref_w, probs = oracle.qmoe_forward(Ls)
+    ids = ti[tidx].cpu().numpy()
+    w = tw[tidx].cpu()
+    near = check_routing(ids, w.numpy(), probs, ref_ids, wl.k)
+    if near.any():
+        ref2, _, _, _ = oracle.qmoe_forward(Ls, forced_ids=ids, forced_w=w.double().numpy())
+        ref[near] = ref2[near]
+    if accumulate:
+        ref = ref + out0[tidx].double().cpu().numpy()
+    if normwise:
+        err = float(np.abs(o[tidx].double().cpu().numpy() - ref).max())
+        bound = 1e-2 * (1.0 + float(np.abs(ref).max()))
+        assert err <= bound, "%s (fast): max err %.4g > %.4g" % (wl.name, err, bound)
+        return err / bound
+    return assert_close_layer(o[tidx], ref, wl.name + " (prefill)")
+
+
+SMALL_CASES = [
+    S.WORKLOADS["tiny"],
+    S.Workload("pf_ragged", 37, 256, 128, 8, 2, 32, S.F16, S.F16, True, -5),
+    S.Workload("pf_multi_tile", 300, 256, 128, 8, 2, 32, S.F16, S.F16, True, -5),
+    S.Workload("pf_bf16_bs64", 100, 512, 384, 16, 4, 64, S.BF16, S.BF16, False, -6),
+    S.Workload("pf_mixed_zp", 64, 512, 256, 16, 4, 32, S.BF16, S.F16, True, -5),
+    S.Workload("pf_f16_bf16s", 48, 384, 192, 12, 3, 64, S.F16, S.BF16, False, -6),
+    S.Workload("pf_bs128", 80, 1024, 640, 32, 4, 128, S.BF16, S.BF16, True, -6),
+    S.Workload("pf_k8_e128", 40, 512, 256, 128, 8, 32, S.BF16, S.BF16, True, -5),
+    S.Workload("pf_e256_k8", 33, 256, 128, 256, 8, 32, S.F16, S.BF16, False, -6),
+    S.Workload("pf_k1", 130, 256, 128, 4, 1, 32, S.F16, S.F16, True, -5),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL_CASES, ids=[w.name for w in SMALL_CASES])
+def test_prefill_matches_oracle(wl):
+    check_prefill(wl, seed=3)
+
+
+def test_prefill_decode_shape_forced():
+    """T = 16 at the full layer size through the grouped GEMM (every token)."""
+    check_prefill(S.WORKLOADS["verify"], seed=5)
+
+
+def test_prefill_full_size_sampled():
+    """T = 512, bf16, block 128, no zero points, Zipf-skewed routing."""
+    check_prefill(S.WORKLOADS["prefill"], seed=1, sample=24)
+
+
+def test_stack_layer_full_size_sampled():
+    """One layer of the T = 2048 stack shape (bf16 tokens, fp16 scales, zp)."""
+    wl = S.WORKLOADS["stack"]
+    check_prefill(wl, seed=2, sample=16)
+
+
+def test_prefill_residual_accumulate():
+    check_prefill(S.Workload("pf_res", 50, 256, 128, 8, 2, 32, S.BF16, S.BF16, True, -5), seed=4,
+                  accumulate=True)
+
+
+def test_prefill_one_expert_gets_every_token():
+    """A large bias sends all 300 tokens to one expert first: that expert
+    needs three token tiles, the rest are thin."""
+    wl = S.Workload("pf_hot", 300, 256, 128, 8, 2, 32, S.F16, S.F16, True, -5)
+    L = S.make_layer(wl, seed=6, device=DEV)
+    bias = torch.zeros(wl.E, device=DEV)
+    bias[5] = 30.0
+    L["router_bias"] = bias
+    check_prefill(wl, L=L)
+
+
+def test_auto_path_above_decode_limit_is_prefill():
+    """T = 17 takes the grouped GEMM under the automatic path choice."""
+    check_prefill(S.Workload("pf_auto", 17, 256, 128, 8, 2, 32, S.F16, S.F16, True, -5), seed=8,
+                  path=B.PATH_AUTO)
+
+
+def test_prefill_repeat_calls_close():
+    """fp32 atomics make the order of the k expert contributions vary, so
+    repeated calls agree to rounding, not bit for bit."""
+    wl = S.Workload("pf_rep", 64, 256, 128, 8, 2, 32, S.BF16, S.BF16, False, -6)
+    L = S.make_layer(wl, seed=9, device=DEV)
+    ws = B.Workspace(wl.T, wl.H, wl.I, wl.E, wl.k)
+    a = B.qmoe_forward(L, ws=ws, path=B.PATH_PREFILL).float()
+    for _ in range(3):
+        b = B.qmoe_forward(L, ws=ws, path=B.PATH_PREFILL).float()
+        assert torch.allclose(a, b, rtol=1e-2, atol=1e-2)
+
+
+def test_prefill_rejects_unsupported_shape():
+    """H not a multiple of 128: the grouped GEMM reports UNSUPPORTED and
+    enqueues nothing."""
+    wl = S.Workload("pf_bad", 20, 320, 96, 8, 2, 32, S.F16, S.F16, True, -5)
+    L = S.make_layer(wl, seed=1, device=DEV)
+    with pytest.raises(RuntimeError, match="unsupported"):
+        B.qmoe_forward(L, path=B.PATH_PREFILL)
+
+
+FAST_CASES = [
+    S.WORKLOADS["tiny"],
+    S.Workload("pf_ragged", 37, 256, 128, 8, 2, 32, S.F16, S.F16, True, -5),
+    S.Workload("pf_multi_tile", 300, 256, 128, 8, 2, 32, S.F16, S.F16, True, -5),
+    S.Workload("pf_bf16_bs64", 100, 512, 384, 16, 4, 64, S.BF16, S.BF16, False, -6),
+    S.Workload("pf_mixed_small", 64, 512, 256, 16, 4, 32, S.BF16, S.F16, True, -7),
+]
+
+
+@pytest.mark.parametrize("wl", FAST_CASES, ids=[w.name for w in FAST_CASES])
+def test_prefill_fast_matches_oracle(wl):
+    check_prefill(wl, seed=3, path=B.PATH_PREFILL_FAST)
+
+
+@pytest.mark.parametrize("name", ["prefill", "stack"])
+def test_prefill_fast_full_size_normwise(name):
+    check_prefill(S.WORKLOADS[name], seed=1, sample=12, path=B.PATH_PREFILL_FAST, normwise=True)
