@@ -173,6 +173,33 @@ int qmoe_forward_profiled(const void* x, int act_dtype, const void* router_w,
                           size_t workspace_bytes, void* stream, void* const* events,
                           int n_events);
 
+/* qmoe_forward without a caller workspace.  An engineering addition with no
+ * counterpart in the method's sources: it serves callers that cannot give
+ * the library device memory, such as a plain C host program with no device
+ * allocator, or a plugin hook that receives no workspace argument and must
+ * not call cudaMalloc (which synchronises the whole device).
+ *
+ * The workspace is a library-owned static device array of
+ * QMOE_NOALLOC_SCRATCH_BYTES (2 MiB) per device; the call allocates
+ * nothing.  Its first 1 KB (the control block: device status word and the
+ * router's grouping counter) starts at zero when the library is loaded and
+ * every call leaves the counter at zero again.  The first call on a device
+ * looks the array's address up (cudaGetSymbolAddress), so make that first
+ * call, with the device current, before any stream capture.
+ *
+ * Same arguments and results as qmoe_forward (path chosen as by
+ * QMOE_PATH_AUTO), minus the workspace.  Shapes whose workspace
+ * (qmoe_workspace_size) exceeds QMOE_NOALLOC_SCRATCH_BYTES return
+ * QMOE_ERR_UNSUPPORTED and enqueue nothing; the Qwen1.5-MoE-A2.7B layer
+ * shape fits up to T = 16.  Overlapping calls on one device (two streams,
+ * or two host threads without ordering) share the array and race: order
+ * them on one stream.  The device status word is not reported here. */
+#define QMOE_NOALLOC_SCRATCH_BYTES (2u << 20)
+int qmoe_forward_noalloc(const void* x, int act_dtype, const void* router_w, const float* router_bias,
+                         qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
+                         int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
+                         int32_t* topk_ids_out, int accumulate, void* stream);
+
 /* DequantizeLinear of one [N, K] matrix (packed [N, K/2]) to fp32 out[N,K]:
  * (q - zp) * scale, which fp32 holds exactly. */
 int qmoe_dequant(const uint8_t* w, const void* scales, int scale_dtype, const uint8_t* zp, int N,

@@ -64,6 +64,9 @@ def lib():
         L.qmoe_forward_profiled.restype = i32
         L.qmoe_forward_profiled.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
             [vp, i32, vp, sz, vp, ctypes.POINTER(ctypes.c_void_p), i32]
+        L.qmoe_forward_noalloc.restype = i32
+        L.qmoe_forward_noalloc.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
+            [vp, vp, vp, i32, vp]
         L.qmoe_dequant.restype = i32
         L.qmoe_dequant.argtypes = [vp, vp, i32, vp, i32, i32, i32, vp, vp]
         L.qmoe_rmsnorm.restype = i32
@@ -168,6 +171,26 @@ def qmoe_forward(layer, x=None, out=None, ws=None, accumulate=False, path=PATH_A
                                T, H, I, E, k, bs, _p(o), _p(tw), _p(ti), int(bool(accumulate)),
                                int(path), ws.ptr, ws.nbytes, _stream())
     _check(rc, "qmoe_forward")
+    return (o, tw, ti) if return_routing else o
+
+
+def qmoe_forward_noalloc(layer, x=None, out=None, accumulate=False, return_routing=False):
+    """qmoe_forward with the library's static device workspace (no caller
+    workspace; calls on one device must not overlap)."""
+    L = layer
+    x = L["x"] if x is None else x
+    T = x.shape[0]
+    H, I, E, k, bs = (int(L[n]) for n in ("H", "I", "E", "k", "block_size"))
+    o = out if out is not None else torch.empty((T, H), dtype=x.dtype, device=x.device)
+    tw = ti = None
+    if return_routing:
+        tw = torch.empty((T, k), dtype=torch.float32, device=x.device)
+        ti = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    rc = lib().qmoe_forward_noalloc(_p(x), _dt(x), _p(L["router_w"]), _p(L.get("router_bias")),
+                                    _qw(L, "gate"), _qw(L, "up"), _qw(L, "down"), _dt(L["gate_s"]),
+                                    T, H, I, E, k, bs, _p(o), _p(tw), _p(ti), int(bool(accumulate)),
+                                    _stream())
+    _check(rc, "qmoe_forward_noalloc")
     return (o, tw, ti) if return_routing else o
 
 

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "launch.h"
 #include "qmoe.h"
 
@@ -361,6 +363,67 @@ int qmoe_get_device_status(void* workspace, uint32_t* bits_out, void* stream) {
   if (bits & QMOE_ST_TIMEOUT) return QMOE_ERR_TIMEOUT;
   if (bits & QMOE_ST_INDEX) return QMOE_ERR_DEVICE_CHECK;
   return QMOE_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------
+// qmoe_forward_noalloc: qmoe_forward with the workspace in a static device
+// array instead of caller memory.  For callers that cannot hand the library
+// device memory: a plain C host program that links only this library and
+// has no device allocator, or a plugin interface whose per-call hook gets
+// no workspace argument and must not call cudaMalloc (which synchronises
+// the device and so stalls every other stream in the process).
+
+namespace {
+
+// 2 MiB: the whole layout of qmoe_workspace_size for the Qwen1.5-MoE-A2.7B
+// layer shape (H = 2048, I = 1408, E = 60, k = 4) at T <= 16 is ~1.3 MB.
+// Zero-initialised at module load, which is what the control block (the
+// first 1 KB: sticky status word and the router's grouping counter) must
+// start as; every call leaves the counter back at zero.
+constexpr size_t kNoAllocScratchBytes = QMOE_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// device address of the scratch array, looked up once per device
+void* noalloc_scratch_ptr(int* rc) {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *rc = QMOE_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *rc = cuda_status(e);
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  *rc = QMOE_OK;
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmoe_forward_noalloc(const void* x, int act_dtype, const void* router_w, const float* router_bias,
+                         qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T, int H,
+                         int I, int E, int k, int block_size, void* out, float* topk_w_out,
+                         int32_t* topk_ids_out, int accumulate, void* stream) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1) return QMOE_ERR_INVALID_ARG;
+  if (ws_layout(T, H, I, E, k).total > kNoAllocScratchBytes) return QMOE_ERR_UNSUPPORTED;
+  int rc = QMOE_OK;
+  void* scratch = noalloc_scratch_ptr(&rc);
+  if (!scratch) return rc;
+  return forward_impl(x, act_dtype, router_w, router_bias, gate, up, down, scale_dtype, T, H, I, E, k,
+                      block_size, out, topk_w_out, topk_ids_out, accumulate, QMOE_PATH_AUTO, scratch,
+                      kNoAllocScratchBytes, stream, nullptr, 0);
 }
 
 }  // extern "C"

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("qmoe_route", "matmul_nbits", "qmoe_forward", "qmoe_forward_ex", "qmoe_dequant",
               "qmoe_rmsnorm", "qmoe_workspace_size", "qmoe_workspace_init", "qmoe_status_string",
-              "qmoe_get_device_status"):
+              "qmoe_get_device_status", "qmoe_forward_noalloc"):
         assert n in names, n
 
 
@@ -125,3 +125,13 @@ def test_oracle_and_product_share_no_code():
     for f in os.listdir(os.path.join(ROOT, "oracle")):
         if f.endswith((".py", ".c")):
             assert "int4_block_quantized_gb300" not in open(os.path.join(ROOT, "oracle", f)).read(), f
+
+
+def test_noalloc_rejects_oversize_shapes_on_the_host(L):
+    """The size check precedes any CUDA call: UNSUPPORTED for a workspace
+    beyond the 2 MiB static array, INVALID_ARG for T = 0."""
+    from int4_block_quantized_gb300.binding import QWeight
+    q = QWeight(FAKE, FAKE, None)
+    args = lambda T: (FAKE, 1, FAKE, None, q, q, q, 1, T, 2048, 1408, 60, 4, 128, FAKE, None, None, 0, None)
+    assert L.qmoe_forward_noalloc(*args(512)) == 2
+    assert L.qmoe_forward_noalloc(*args(0)) == 1
