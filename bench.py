@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "QMoE layer tokens/s; decode HBM GB/s and prefill TFLOPS as % of GB300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24}
-DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 240}
+DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 60}
 
 
 def parse():
@@ -142,8 +142,13 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
+def is_decode(wl):
+    return wl.T <= 16
+
+
 def workload_bytes(wl, D):
-    """Algorithmic bytes: weights of the D distinct selected experts, router, x, out."""
+    """Algorithmic bytes and FLOPs of one layer: weights of the D distinct
+    selected experts, router, x in, out; per kernel the same for its share."""
     from int4_block_quantized_gb300 import synthetic as S
     A = wl.T * wl.k
     nbh, nbi = wl.H // wl.block_size, wl.I // wl.block_size
@@ -154,14 +159,21 @@ def workload_bytes(wl, D):
     router = wl.H * wl.E * 2 + (wl.E * 4 if wl.zipf_s else 0)
     xio = 2 * wl.T * wl.H * 2
     layer = D * (gu + dn) + router + xio
-    gateup_kernel = D * gu + wl.T * wl.H * 2 + A * wl.I * 4    # x in, fp32 act out
-    down_kernel = D * dn + A * wl.I * 4 + wl.T * wl.H * 2      # act in, out
+    if is_decode(wl):
+        gateup_kernel = D * gu + wl.T * wl.H * 2 + A * wl.I * 4    # x in, fp32 act out
+        down_kernel = D * dn + A * wl.I * 4 + wl.T * wl.H * 2      # act in, out
+    else:
+        gateup_kernel = D * gu + A * wl.H * 2 + A * wl.I * 2       # gathered x in, act out
+        down_kernel = D * dn + A * wl.I * 2 + wl.T * wl.H * 4      # act in, fp32 sum out
     flops = 2 * A * 3 * wl.H * wl.I + 2 * wl.T * wl.H * wl.E
-    return dict(layer=layer, gateup=gateup_kernel, down=down_kernel, flops=flops)
+    return dict(layer=layer, gateup=gateup_kernel, down=down_kernel, flops=flops,
+                gateup_flops=2 * A * 2 * wl.H * wl.I, down_flops=2 * A * wl.H * wl.I)
 
 
 def cpu_baseline(wl, layer_cpu, xs_cpu, budget_s=12.0):
-    """The oracle as it stands, single-threaded, on a bounded sample of tokens."""
+    """The oracle as it stands, single-threaded, on a bounded sample of tokens
+    through one layer; for the stack the rate is divided by its layer count
+    (every layer has the same shape and cost)."""
     import oracle
     t0 = time.perf_counter()
     tokens = 0
@@ -174,42 +186,61 @@ def cpu_baseline(wl, layer_cpu, xs_cpu, budget_s=12.0):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return tokens / el, tokens, el
+    return tokens / el / wl.layers, tokens, el
 
 
 def run_reference(a, wl):
-    """--impl reference: the fp64 oracle on the host cores, same workload."""
+    """--impl reference: the fp64 oracle on the host cores, same workload.
+    A step pushes a bounded sample of the batch's tokens through the whole
+    path (for the stack: RMSNorm + layer, 24 times, alternating between two
+    generated weight sets of the stack's shape)."""
+    import numpy as np
     import torch
     from int4_block_quantized_gb300 import synthetic as S
     import oracle
     oracle._load()
-    layer = S.make_weights(wl, seed=0, device="cpu", layer=0)
-    T1 = min(wl.T, 1 if wl.T <= 16 else 4)  # one step = a bounded sample of the batch
-    xs = [S.make_x(wl, seed=0, device="cpu", T=T1, layer=l) for l in range(4)]
+    nw = 2 if wl.layers > 1 else 1
+    layers = [S.make_weights(wl, seed=0, device="cpu", layer=l) for l in range(nw)]
+    T1 = min(wl.T, 1 if wl.T <= 16 else 2)  # one step = a bounded sample of the batch
+    xs = [S.make_x(wl, seed=0, device="cpu", layer=l)[:T1].contiguous() for l in range(4)]
+    tdt = torch.bfloat16 if wl.act_dtype else torch.float16
+
+    def one_step(i):
+        x = xs[i % 4]
+        if wl.layers == 1:
+            oracle.qmoe_forward(dict(layers[0], x=x, T=T1))
+            return
+        xd = x.to(torch.float64)
+        for l in range(wl.layers):
+            xn = oracle.rmsnorm(torch.from_numpy(xd.numpy()).to(tdt), wl.act_dtype, T1, wl.H, 1e-6)
+            xn16 = torch.from_numpy(xn).to(tdt)
+            y, _, _, _ = oracle.qmoe_forward(dict(layers[l % nw], x=xn16, T=T1))
+            xd = torch.from_numpy(xd.numpy() + y)
+
     budget = 150.0
-    # warm-up steps (untimed), then timed steps within the budget
     tw0 = time.perf_counter()
     for i in range(a.warmup):
-        oracle.qmoe_forward(dict(layer, x=xs[i % 4], T=T1))
+        one_step(i)
         if time.perf_counter() - tw0 > 20.0:
             break
     t0 = time.perf_counter()
     steps = 0
     while steps < a.steps:
-        oracle.qmoe_forward(dict(layer, x=xs[steps % 4], T=T1))
+        one_step(steps)
         steps += 1
         if time.perf_counter() - t0 > budget:
             break
     el = time.perf_counter() - t0
     v = steps * T1 / el
+    sample = "%d step(s) of %d token(s) of the %s workload through %s (all %d experts resident), fp64, one thread" % (
+        steps, T1, wl.name, "one layer" if wl.layers == 1 else
+        "%d layers of RMSNorm + layer (two weight sets alternating)" % wl.layers, wl.E)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": a.gpus,
         "steps": steps, "warmup": a.warmup, "ms_per_step": 1000.0 * el / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(wl, a),
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d step(s) of %d token(s) of the %s workload through one layer "
-                                   "(all %d experts resident), fp64, one thread" % (steps, T1, wl.name, wl.E)},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -225,6 +256,10 @@ def config_dict(wl, a):
         "parallelism": "replicas x%d" % a.gpus}
 
 
+KERNELS = {True: ["route", "gateup", "down"],
+           False: ["route", "permute", "gateup", "down", "convert"]}
+
+
 def run_ours(a, wl):
     import torch
     from int4_block_quantized_gb300 import binding as B
@@ -232,20 +267,40 @@ def run_ours(a, wl):
     rank, world, local = dist_init()
     dev = torch.device("cuda", local)
     B.lib()
+    dec = is_decode(wl)
+    stack = wl.layers > 1
+    names = KERNELS[dec]
     P = a.pool or POOL[wl.name]
+    if stack:
+        P = wl.layers  # the stack itself: every step runs all its layers
     layers = [S.make_weights(wl, seed=0, device=dev, layer=l) for l in range(P)]
-    xs = [S.make_x(wl, seed=0, device=dev, layer=l) for l in range(P)]
+    if stack:
+        xs = [S.make_x(wl, seed=0, device=dev, layer=0)]
+        xbuf = torch.empty_like(xs[0])
+        xn = torch.empty_like(xs[0])
+    else:
+        xs = [S.make_x(wl, seed=0, device=dev, layer=l) for l in range(P)]
     outs = [torch.empty_like(x) for x in xs]
     ws = B.Workspace(wl.T, wl.H, wl.I, wl.E, wl.k, device=dev)
     # distinct experts per pool layer (for the algorithmic byte count)
     Ds = []
     for l in range(P):
-        _, ti, _, _ = B.qmoe_route(xs[l], layers[l]["router_w"], wl.k, layers[l]["router_bias"], ws=ws)
+        _, ti, _, _ = B.qmoe_route(xs[l % len(xs)], layers[l]["router_w"], wl.k, layers[l]["router_bias"], ws=ws)
         Ds.append(int(torch.unique(ti).numel()))
     D_mean = sum(Ds) / len(Ds)
     wb = workload_bytes(wl, D_mean)
+    launches_per_step = wl.layers * (len(names) + (1 if stack else 0))
+
+    def run_stack(x_in, x_out):
+        x_out.copy_(x_in)
+        for l in range(wl.layers):
+            B.qmoe_rmsnorm(x_out, out=xn)
+            B.qmoe_forward(layers[l], x=xn, out=x_out, ws=ws, accumulate=True)
 
     def step(i):
+        if stack:
+            run_stack(xs[0], xbuf)
+            return
         j = i % P
         B.qmoe_forward(layers[j], x=xs[j], out=outs[j], ws=ws)
 
@@ -255,7 +310,7 @@ def run_ours(a, wl):
         for i in range(3):
             step(i)
     torch.cuda.synchronize(dev)
-    G = min(a.steps, 24 * P if wl.T <= 16 else 2 * P)
+    G = min(a.steps, 24 * P if dec else (4 if stack else 2 * P))
 
     def capture(n, start):
         g = torch.cuda.CUDAGraph()
@@ -295,8 +350,9 @@ def run_ours(a, wl):
     # ---- per-kernel durations for the roofline: events between the kernels
     # (no programmatic overlap), replayed from a CUDA graph so host launch
     # gaps are not measured
-    nk = 3
-    nrep = 3
+    nk = len(names)
+    nrep = 3 if dec else 2
+    xprof = [xn.copy_(B.qmoe_rmsnorm(xs[0])) if stack else None]
     evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(nrep * P)]
     with torch.cuda.stream(s):
         for evs in evsets:  # torch creates the CUDA event on first record
@@ -307,14 +363,30 @@ def run_ours(a, wl):
     with torch.cuda.graph(g_prof, stream=s):
         for i, evs in enumerate(evsets):
             j = i % P
-            B.qmoe_forward_profiled(layers[j], evs, x=xs[j], out=outs[j], ws=ws)
+            if stack:
+                B.qmoe_forward_profiled(layers[j], evs, x=xprof[0], out=outs[0], ws=ws)
+            else:
+                B.qmoe_forward_profiled(layers[j], evs, x=xs[j], out=outs[j], ws=ws)
     g_prof.replay()
     torch.cuda.synchronize(dev)
     g_prof.replay()
     torch.cuda.synchronize(dev)
     kms = [statistics.mean(evs[kk].elapsed_time(evs[kk + 1]) for evs in evsets[P:]) for kk in range(nk)]
+    kdict = dict(zip(names, kms))
     pk = peaks()
-    gu_gbs = wb["gateup"] / (kms[1] * 1e-3) / 1e9
+    gu_ms = kdict["gateup"]
+    gu_gbs = wb["gateup"] / (gu_ms * 1e-3) / 1e9
+    gu_tfs = wb["gateup_flops"] / (gu_ms * 1e-3) / 1e12
+    if dec or wb["gateup"] / pk["hbm_gbs"] / 1e9 >= wb["gateup_flops"] / pk["bf16_tflops"] / 1e12:
+        roof = {"bound": "hbm", "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": gu_gbs / pk["hbm_gbs"], "other": {"tflops": gu_tfs, "tensor_frac": gu_tfs / pk["bf16_tflops"]}}
+    else:
+        roof = {"bound": "tensor", "achieved": gu_tfs, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": gu_tfs / pk["bf16_tflops"], "other": {"gbs": gu_gbs, "hbm_frac": gu_gbs / pk["hbm_gbs"]}}
+    roof.update({"traffic": None, "peak_source": pk["source"] + (" (copy GB/s)" if roof["bound"] == "hbm"
+                                                                 else " (bf16 burst)"),
+                 "kernel": "decode gate-up (+SwiGLU)" if dec else "grouped GEMM gate-up (+SwiGLU), exact hi+lo operands",
+                 "bytes_per_launch": wb["gateup"], "flops_per_launch": wb["gateup_flops"], "launch_ms": gu_ms})
 
     # ---- end to end through the public API: pinned H2D of x, forward, D2H of out
     xh = [x.cpu().pin_memory() for x in xs]
@@ -322,21 +394,26 @@ def run_ours(a, wl):
     xd = torch.empty_like(xs[0])
     od = torch.empty_like(xs[0])
     n_e2e = min(a.steps, 4000)
+
+    def e2e_step(i):
+        j = i % len(xs)
+        xd.copy_(xh[j], non_blocking=True)
+        if stack:
+            run_stack(xd, od)
+        else:
+            B.qmoe_forward(layers[i % P], x=xd, out=od, ws=ws)
+        oh[j].copy_(od, non_blocking=True)
+
     with torch.cuda.stream(s):
         for i in range(3):
-            xd.copy_(xh[i % P], non_blocking=True)
-            B.qmoe_forward(layers[i % P], x=xd, out=od, ws=ws)
-            oh[i % P].copy_(od, non_blocking=True)
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         barrier(world)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(s)
         for i in range(n_e2e):
-            j = i % P
-            xd.copy_(xh[j], non_blocking=True)
-            B.qmoe_forward(layers[j], x=xd, out=od, ws=ws)
-            oh[j].copy_(od, non_blocking=True)
+            e2e_step(i)
         f1.record(s)
     f1.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
@@ -345,34 +422,36 @@ def run_ours(a, wl):
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         lc = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in layers[0].items()}
-        xc = [x.cpu() for x in xs[:4]]
+        nt = wl.T if dec else 2  # tokens per oracle call: a bounded sample of the batch
+        xc = [x.cpu()[:nt].contiguous() for x in xs[:4]]
+        if stack:
+            xc = [B.qmoe_rmsnorm(xs[0][i * nt:(i + 1) * nt].contiguous()).cpu() for i in range(4)]
         v, toks, el = cpu_baseline(wl, lc, xc)
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": "%d token(s) of the %s workload through one layer in %.1f s, fp64, one thread"
-                         % (toks, wl.name, el)}
+               "sample": "%d token(s) of the %s workload through one layer in %.1f s, fp64, one thread%s"
+                         % (toks, wl.name, el, "; rate divided by the %d layers" % wl.layers if stack else "")}
 
     if rank == 0:
         ms_step = ms / a.steps
+        ms_layer = ms_step / wl.layers
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp16" if wl.act_dtype == 0 else "bf16",
             "data": "synthetic", "config": config_dict(wl, a),
-            "roofline": {"bound": "hbm", "kernel": "decode gate-up (+SwiGLU)",
-                         "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gu_gbs / pk["hbm_gbs"], "traffic": None,
-                         "peak_source": pk["source"],
-                         "bytes_per_launch": wb["gateup"], "launch_ms": kms[1]},
-            "layer": {"bytes": wb["layer"], "distinct_experts": D_mean,
-                      "hbm_gbs": wb["layer"] / (ms_step * 1e-3) / 1e9,
-                      "hbm_frac": wb["layer"] / (ms_step * 1e-3) / 1e9 / pk["hbm_gbs"],
-                      "kernel_ms": {"route": kms[0], "gateup": kms[1], "down": kms[2]},
-                      "tflops": wb["flops"] / (ms_step * 1e-3) / 1e12},
+            "roofline": roof,
+            "layer": {"path": "decode" if dec else "prefill (exact hi+lo operands)",
+                      "bytes": wb["layer"], "distinct_experts": D_mean, "ms": ms_layer,
+                      "hbm_gbs": wb["layer"] / (ms_layer * 1e-3) / 1e9,
+                      "hbm_frac": wb["layer"] / (ms_layer * 1e-3) / 1e9 / pk["hbm_gbs"],
+                      "tflops": wb["flops"] / (ms_layer * 1e-3) / 1e12,
+                      "tensor_frac": wb["flops"] / (ms_layer * 1e-3) / 1e12 / pk["bf16_tflops_sustained"],
+                      "kernel_ms": kdict},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,
                     "steps": n_e2e},
-            "gpu_launches": 3 * a.steps,
+            "gpu_launches": launches_per_step * a.steps,
             "clocks": {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
                        "samples": ck["samples"]},
         }

@@ -222,7 +222,10 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   int ev_i = 0;
   auto mark = [&]() -> int {
     if (events && ev_i < n_events && events[ev_i])
-      if (cudaEventRecord((cudaEvent_t)events[ev_i], st) != cudaSuccess) return QMOE_ERR_CUDA;
+      // external: under stream capture the record becomes a graph node that
+      // timing can read (a plain record would only order the capture)
+      if (cudaEventRecordWithFlags((cudaEvent_t)events[ev_i], st, cudaEventRecordExternal) != cudaSuccess)
+        return QMOE_ERR_CUDA;
     ++ev_i;
     return QMOE_OK;
   };
