@@ -221,11 +221,18 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   const bool pdl = events == nullptr;
   int ev_i = 0;
   auto mark = [&]() -> int {
-    if (events && ev_i < n_events && events[ev_i])
-      // external: under stream capture the record becomes a graph node that
-      // timing can read (a plain record would only order the capture)
-      if (cudaEventRecordWithFlags((cudaEvent_t)events[ev_i], st, cudaEventRecordExternal) != cudaSuccess)
-        return QMOE_ERR_CUDA;
+    if (events && ev_i < n_events && events[ev_i]) {
+      // under stream capture the record must be external to become a graph
+      // node that timing can read (a plain record only orders the capture);
+      // outside capture the flag is not accepted
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(st, &cs);
+      if (e == cudaSuccess)
+        e = cs == cudaStreamCaptureStatusActive
+                ? cudaEventRecordWithFlags((cudaEvent_t)events[ev_i], st, cudaEventRecordExternal)
+                : cudaEventRecord((cudaEvent_t)events[ev_i], st);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
     ++ev_i;
     return QMOE_OK;
   };

@@ -156,7 +156,7 @@ struct PrefillParams {
   int32_t* tiles;           // [ntiles][4]
   uint32_t* ctl;            // control block (status, tile count)
   int accumulate;
-  int nst, nsz;             // pipeline stages, tile scale buffers (set per GEMM launch)
+  int nst, nsz, npk;        // operand stages, tile scale buffers, packed-code slots (per GEMM launch)
 };
 
 }  // namespace qmoe

@@ -39,8 +39,7 @@
 
 namespace qmoe {
 
-constexpr int kGemmThreads = 320;  // 10 warps
-constexpr int kStages = 4;
+constexpr int kGemmThreads = 512;  // 16 warps (roles listed at the kernel)
 constexpr int kBN = 128;           // max tokens per tile (TMEM columns per accumulator)
 constexpr int kBoxRows = 32;       // token rows per B TMA box
 constexpr int kModeGU = 0, kModeDN = 1;
@@ -226,40 +225,56 @@ __device__ __forceinline__ void split_act(float a, uint16_t& h, uint16_t& l) {
 
 // ------------------------------------------------------------ grouped GEMM
 constexpr uint32_t kTileOp = 128 * 128;    // 16-bit operand tile: 128 rows x 64 K (SW128)
-constexpr uint32_t kStagePk = 128 * 32;    // packed codes: 128 rows x 64 codes
+constexpr uint32_t kPkBytes = 128 * 32;    // packed codes: 128 rows x 64 codes
+constexpr int kMaxPk = 24;                 // packed-code ring slots (at most)
 constexpr uint32_t kGbufFloats = 64 * 17;  // gate values of one 16-column chunk (padded rows)
 constexpr uint32_t kTmemCols = 256;        // two 128-column accumulators
 constexpr uint32_t kSmemLimit = 232448;    // 227 KB per CTA
+constexpr int kDeqWarps = 8;               // two per SM sub-partition: row = warp%4*32+lane, half = K half
 
-// Stage: [A hi][A lo (split)][B hi][B lo (split down)][packed codes]
+// Warp roles (kGemmThreads = 512):
+//   0      token-tile producer (TMA, L2-resident gathered tokens / SwiGLU output)
+//   1      TMEM owner and tcgen05.mma issuer
+//   2      weight producer: packed codes (deep ring) and each tile's scales / zero points
+//   3      idle
+//   4-11   dequantisers
+//   12-15  epilogue (TMEM lane quadrant = warp % 4)
+// Shared memory: [barriers][scale buffers][operand stages: A hi, A lo, B hi, B lo][packed ring][exchange]
 struct GemmSmem {
-  uint32_t a_lo, b_hi, b_lo, pk, stage;  // offsets inside a stage, stage size
-  uint32_t sz_bytes, sz_off, stage_off, gbuf_off, total;
+  uint32_t a_lo, b_hi, b_lo, stage;  // offsets inside an operand stage, stage size
+  uint32_t sz_bytes, sz_off, stage_off, pk_off, gbuf_off, total;
 };
-__host__ __device__ inline GemmSmem gemm_smem(int mode, bool split, int nb, bool has_zp, int nst, int nsz) {
+__host__ __device__ inline GemmSmem gemm_smem(int mode, bool split, int nb, bool has_zp, int nst, int nsz, int npk) {
   GemmSmem S;
   const uint32_t na = split ? 2 : 1, nbt = (split && mode == kModeDN) ? 2 : 1;
   S.a_lo = kTileOp;
   S.b_hi = na * kTileOp;
   S.b_lo = S.b_hi + kTileOp;
-  S.pk = S.b_hi + nbt * kTileOp;
-  S.stage = S.pk + kStagePk;
+  S.stage = S.b_hi + nbt * kTileOp;
   S.sz_bytes = ((uint32_t)128 * nb * 2 + (has_zp ? (uint32_t)128 * nb : 0u) + 1023u) & ~1023u;
   S.sz_off = 1024;
   S.stage_off = S.sz_off + nsz * S.sz_bytes;
-  S.gbuf_off = S.stage_off + nst * S.stage;
+  S.pk_off = S.stage_off + nst * S.stage;
+  S.gbuf_off = S.pk_off + npk * kPkBytes;
   S.total = S.gbuf_off + (mode == kModeGU ? 2 * kGbufFloats * 4 : 0) + 1024;  // + base alignment slack
   return S;
 }
-// deepest pipeline that fits (4..2 stages); at equal depth two tile-scale buffers
-__host__ inline bool gemm_plan(int mode, bool split, int nb, bool has_zp, int& nst, int& nsz) {
-  for (int st = kStages; st >= 2; --st)
-    for (int sz = 2; sz >= 1; --sz)
-      if (gemm_smem(mode, split, nb, has_zp, st, sz).total <= kSmemLimit) {
+// Pipeline plan.  Two tile-scale buffers first (with one, the weight
+// producer cannot start the next tile's codes until the current tile is
+// dequantised), then 3 operand stages if at least 8 packed slots remain,
+// else 2; the packed ring takes the rest (<= 24 slots).
+__host__ inline bool gemm_plan(int mode, bool split, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
+  for (int sz = 2; sz >= 1; --sz)
+    for (int st = 3; st >= 2; --st) {
+      int pk = kMaxPk;
+      while (pk >= 8 && gemm_smem(mode, split, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
+      if (pk >= 8) {
         nst = st;
         nsz = sz;
+        npk = pk;
         return true;
       }
+    }
   return false;
 }
 
@@ -294,6 +309,13 @@ struct Ring {
   }
 };
 
+// drain helper for the abort path: wait (bounded) for the last use of each
+// slot of a ring whose `issued` uses went round-robin over n slots
+__device__ __forceinline__ void drain_ring(uint64_t* full, int n, int issued) {
+  for (int s = 0; s < n; ++s)
+    if (issued > s) mbar_wait(&full[s], ((issued - 1 - s) / n) & 1, nullptr);
+}
+
 // One persistent CTA per SM.  Work item t = (weight row block mb, token
 // tile nt), nt fastest, so the token tiles of one expert run side by side
 // and share the weight tile through L2.
@@ -309,13 +331,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int K = GU ? p.H : p.I;       // reduction length
   const int NR = GU ? p.I : p.H;      // weight rows per expert matrix
   const int nb = K >> p.lbs;
-  const int nst = p.nst, nsz = p.nsz;
-  const GemmSmem L = gemm_smem(MODE, SPLIT, nb, HAS_ZP, nst, nsz);
+  const int nst = p.nst, nsz = p.nsz, npk = p.npk;
+  const GemmSmem L = gemm_smem(MODE, SPLIT, nb, HAS_ZP, nst, nsz, npk);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* tma_full = bars;                // [kStages] packed codes + tokens landed
-  uint64_t* a_full = bars + kStages;        // [kStages] operand dequantised
-  uint64_t* empty = bars + 2 * kStages;     // [kStages] MMAs done with the stage
-  uint64_t* tmem_full = bars + 3 * kStages; // [2] accumulator complete
+  uint64_t* b_full = bars;                  // [4] token tile landed
+  uint64_t* a_full = bars + 4;              // [4] operand dequantised (one arrival per dequant warp)
+  uint64_t* empty = bars + 8;               // [4] MMAs done with the operand stage
+  uint64_t* pk_full = bars + 12;            // [kMaxPk] packed codes landed
+  uint64_t* pk_empty = pk_full + kMaxPk;    // [kMaxPk] packed codes read
+  uint64_t* tmem_full = pk_empty + kMaxPk;  // [2] accumulator complete
   uint64_t* tmem_empty = tmem_full + 2;     // [2] accumulator drained
   uint64_t* sz_full = tmem_empty + 2;       // [2] tile scales landed
   uint64_t* sz_empty = sz_full + 2;         // [2] tile scales no longer read
@@ -326,6 +350,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   uint8_t* szbuf = smem + L.sz_off;
   uint8_t* stages = smem + L.stage_off;
+  uint8_t* pkbuf = smem + L.pk_off;
   float* gbuf = reinterpret_cast<float*>(smem + L.gbuf_off);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -334,18 +359,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int MB = NR / (GU ? 64 : 128);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&tma_full[s], 1);
-      mbar_init(&a_full[s], 128);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&a_full[s], kDeqWarps);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kMaxPk; ++s) {
+      mbar_init(&pk_full[s], 1);
+      mbar_init(&pk_empty[s], kDeqWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], 128);
+      mbar_init(&tmem_empty[b], 4);
       mbar_init(&sz_full[b], 1);
-      mbar_init(&sz_empty[b], 128);
-      mbar_init(&gx_full[b], 64);
-      mbar_init(&gx_empty[b], 64);
+      mbar_init(&sz_empty[b], kDeqWarps);
+      mbar_init(&gx_full[b], 2);
+      mbar_init(&gx_empty[b], 2);
     }
     mbar_init(fin, 1);
     *s_abort = 0;
@@ -366,16 +395,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
 
   if (warp == 0) {
-    // ============================================================ producer
+    // ============================================================ token-tile producer
     if (lane == 0) {
-      int it = 0, tc = 0;
-      Ring rs, rz;
+      int it = 0;
+      Ring rs;
+      for (int t = blockIdx.x; t < ntile_total && !*s_abort; t += gridDim.x) {
+        const int4 tl = __ldcg(tiles + t % NT);
+        const int row0 = tl.y, npad = (tl.z + 15) & ~15;
+        const int nbox = (npad + kBoxRows - 1) / kBoxRows;
+        const uint32_t btx = nbox * kBoxRows * 128 * (BLO ? 2 : 1);
+        for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst)) {
+          if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) break;
+          uint8_t* st = stages + rs.i * L.stage;
+          uint64_t* fb = &b_full[rs.i];
+          mbar_arrive_expect_tx(fb, btx);
+          for (int bx = 0; bx < nbox; ++bx) {
+            tma_load_2d(st + L.b_hi + bx * kBoxRows * 128, &tm_b, kc * 64, row0 + bx * kBoxRows, fb);
+            if (BLO) tma_load_2d(st + L.b_lo + bx * kBoxRows * 128, &tm_b2, kc * 64, row0 + bx * kBoxRows, fb);
+          }
+        }
+      }
+      if (*s_abort) drain_ring(b_full, nst, it);
+    }
+  } else if (warp == 2) {
+    // ============================================================ weight producer
+    if (lane == 0) {
+      int ip = 0, tc = 0;
+      Ring rp, rz;
       const uint32_t sbytes = 128u * nb * 2, zbytes = HAS_ZP ? 128u * nb : 0u;
       for (int t = blockIdx.x; t < ntile_total && !*s_abort; t += gridDim.x, ++tc, rz.next(nsz)) {
         const int4 tl = __ldcg(tiles + t % NT);
-        const int mb = t / NT;
-        const int e = tl.x, row0 = tl.y, npad = (tl.z + 15) & ~15;
-        const int nbox = (npad + kBoxRows - 1) / kBoxRows;
+        const int mb = t / NT, e = tl.x;
         if (tc >= nsz && !wait_or_abort(&sz_empty[rz.i], rz.ph ^ 1u, status, s_abort)) break;
         // block scales / zero points of the tile's 128 weight rows over the whole K
         uint8_t* sz = szbuf + rz.i * L.sz_bytes;
@@ -394,29 +444,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           bulk_g2s(sz, static_cast<const uint8_t*>(p.s[2]) + r * nb * 2, sbytes, zb);
           if (HAS_ZP) bulk_g2s(sz + sbytes, p.z[2] + r * nb, zbytes, zb);
         }
-        const uint32_t btx = nbox * kBoxRows * 128 * (BLO ? 2 : 1);
-        for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst)) {
-          if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) break;
-          uint8_t* st = stages + rs.i * L.stage;
-          uint64_t* fb = &tma_full[rs.i];
-          mbar_arrive_expect_tx(fb, kStagePk + btx);
+        for (int kc = 0; kc < KC; ++kc, ++ip, rp.next(npk)) {
+          if (ip >= npk && !wait_or_abort(&pk_empty[rp.i], rp.ph ^ 1u, status, s_abort)) break;
+          uint8_t* pk = pkbuf + rp.i * kPkBytes;
+          uint64_t* fb = &pk_full[rp.i];
+          mbar_arrive_expect_tx(fb, kPkBytes);
           if (GU) {
-            tma_load_2d(st + L.pk, &tm_a0, kc * 32, e * NR + mb * 64, fb);
-            tma_load_2d(st + L.pk + 64 * 32, &tm_a1, kc * 32, e * NR + mb * 64, fb);
+            tma_load_2d(pk, &tm_a0, kc * 32, e * NR + mb * 64, fb);
+            tma_load_2d(pk + 64 * 32, &tm_a1, kc * 32, e * NR + mb * 64, fb);
           } else {
-            tma_load_2d(st + L.pk, &tm_a0, kc * 32, e * NR + mb * 128, fb);
-          }
-          for (int bx = 0; bx < nbox; ++bx) {
-            tma_load_2d(st + L.b_hi + bx * kBoxRows * 128, &tm_b, kc * 64, row0 + bx * kBoxRows, fb);
-            if (BLO) tma_load_2d(st + L.b_lo + bx * kBoxRows * 128, &tm_b2, kc * 64, row0 + bx * kBoxRows, fb);
+            tma_load_2d(pk, &tm_a0, kc * 32, e * NR + mb * 128, fb);
           }
         }
       }
       if (*s_abort) {  // let the copies already issued land before the CTA exits
-        for (int s = 0; s < nst; ++s)
-          if (it > s) mbar_wait(&tma_full[s], ((it - 1 - s) / nst) & 1, nullptr);
-        for (int b = 0; b < nsz; ++b)
-          if (tc > b) mbar_wait(&sz_full[b], ((tc - 1 - b) / nsz) & 1, nullptr);
+        drain_ring(pk_full, npk, ip);
+        drain_ring(sz_full, nsz, tc);
       }
     }
   } else if (warp == 1) {
@@ -435,7 +478,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d_tmem = tmem_base + b * kBN;
         bool ok = true;
         for (int kc = 0; kc < KC; ++kc, rs.next(nst)) {
-          if (!wait_or_abort(&a_full[rs.i], rs.ph, status, s_abort)) { ok = false; break; }
+          if (!wait_or_abort(&a_full[rs.i], rs.ph, status, s_abort) ||
+              !wait_or_abort(&b_full[rs.i], rs.ph, status, s_abort)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t st = smem_u32(stages + rs.i * L.stage);
           const uint64_t ah = sw128_desc(st), al = sw128_desc(st + L.a_lo);
@@ -457,55 +504,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_wait(fin, 0, nullptr);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp >= 4 && warp < 4 + kDeqWarps) {
     // ============================================================ dequantisers
     const int r = (warp & 3) * 32 + lane;  // weight row of the tile
-    Ring rs, rz;
-    for (int t = blockIdx.x; t < ntile_total; t += gridDim.x, rz.next(nsz)) {
+    const int hh = (warp - 4) >> 2;        // which 32 codes of the 64-wide chunk
+    int it = 0;
+    Ring rs, rp, rz;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x, rz.next(nsz)) {
       if (!wait_or_abort(&sz_full[rz.i], rz.ph, status, s_abort)) break;
       const uint8_t* sz = szbuf + rz.i * L.sz_bytes;
       const uint16_t* srow = reinterpret_cast<const uint16_t*>(sz) + (size_t)r * nb;
       const uint8_t* zrow = sz + 128u * nb * 2 + (size_t)r * nb;
-      bool ok = true;
-      for (int kc = 0; kc < KC; ++kc, rs.next(nst)) {
-        if (!wait_or_abort(&tma_full[rs.i], rs.ph, status, s_abort)) { ok = false; break; }
+      for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst), rp.next(npk)) {
+        if (!wait_or_abort(&pk_full[rp.i], rp.ph, status, s_abort)) { ok = false; break; }
+        const uint4 q = *reinterpret_cast<const uint4*>(pkbuf + rp.i * kPkBytes + r * 32 + hh * 16);
+        // block_size >= 32: the 32 codes of this half share one block
+        const int blk = (kc * 64 + hh * 32) >> p.lbs;
+        Deq<TA, TS> d;
+        d.set(HAS_ZP ? (uint32_t)zrow[blk] : 8u, srow[blk]);
+        if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) { ok = false; break; }
         uint8_t* st = stages + rs.i * L.stage;
-        const uint4* pk = reinterpret_cast<const uint4*>(st + L.pk + r * 32);
-        const uint4 q0 = pk[0], q1 = pk[1];
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        // block_size >= 32: codes 0-31 of the chunk share one block, 32-63 one block
-        const int blo = (kc * 64) >> p.lbs, bhi = (kc * 64 + 32) >> p.lbs;
-        Deq<TA, TS> dq[2];
-        dq[0].set(HAS_ZP ? (uint32_t)zrow[blo] : 8u, srow[blo]);
-        dq[1].set(HAS_ZP ? (uint32_t)zrow[bhi] : 8u, srow[bhi]);
         const uint32_t roff = (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const Deq<TA, TS>& d = dq[g >> 2];
+        for (int gg = 0; gg < 4; ++gg) {
+          const int g = hh * 4 + gg;
           const uint32_t off = roff + ((g ^ (r & 7)) << 4);  // 128-byte swizzle
           uint4 h, l;  // elements (0,4), (1,5), (2,6), (3,7) of the group
           if (SPLIT) {
-            d.both(w[g], h.x, l.x);
-            d.both(w[g] >> 4, h.y, l.y);
-            d.both(w[g] >> 8, h.z, l.z);
-            d.both(w[g] >> 12, h.w, l.w);
+            d.both(w[gg], h.x, l.x);
+            d.both(w[gg] >> 4, h.y, l.y);
+            d.both(w[gg] >> 8, h.z, l.z);
+            d.both(w[gg] >> 12, h.w, l.w);
             *reinterpret_cast<uint4*>(st + off) = h;
             *reinterpret_cast<uint4*>(st + L.a_lo + off) = l;
           } else {
-            h.x = d.hi(w[g]);
-            h.y = d.hi(w[g] >> 4);
-            h.z = d.hi(w[g] >> 8);
-            h.w = d.hi(w[g] >> 12);
+            h.x = d.hi(w[gg]);
+            h.y = d.hi(w[gg] >> 4);
+            h.z = d.hi(w[gg] >> 8);
+            h.w = d.hi(w[gg] >> 12);
             *reinterpret_cast<uint4*>(st + off) = h;
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&a_full[rs.i]);
+        __syncwarp();
+        // the packed slot is handed back only once the operand it produced is
+        // written: releasing it right after the load let the next TMA fill
+        // race with this chunk on the GPU (wrong rows in a few tiles)
+        if (lane == 0) {
+          mbar_arrive(&a_full[rs.i]);
+          mbar_arrive(&pk_empty[rp.i]);
+        }
       }
       if (!ok) break;
-      mbar_arrive(&sz_empty[rz.i]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sz_empty[rz.i]);
     }
-  } else {
+  } else if (warp >= 12) {
     // ============================================================ epilogue
     const int q = warp & 3;         // TMEM lane quadrant this warp may read
     const int row = q * 32 + lane;  // accumulator row = weight row of the tile
@@ -530,7 +586,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (cc >= 2 && !wait_or_abort(&gx_empty[xb], ((cc >> 1) - 1) & 1, status, s_abort)) { ok = false; break; }
 #pragma unroll
             for (int j = 0; j < 16; ++j) gx[row * 17 + j] = __uint_as_float(v[j]);
-            mbar_arrive(&gx_full[xb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&gx_full[xb]);
           } else {
             if (!wait_or_abort(&gx_full[xb], (cc >> 1) & 1, status, s_abort)) { ok = false; break; }
             const int i = row - 64;
@@ -552,22 +609,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
               }
             }
-            mbar_arrive(&gx_empty[xb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&gx_empty[xb]);
           }
         } else {
+          // lanes 0-15 fetch the chunk's 16 assignments and routing weights
+          int a_l = 0;
+          float w_l = 0.f;
+          if (lane < 16 && c0 + lane < nrows) {
+            a_l = __ldg(p.perm + row0 + c0 + lane);
+            w_l = __ldg(p.topk_w + a_l);
+          }
           const int h = mb * 128 + row;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (c0 + j < nrows) {
-              const int a = __ldg(p.perm + row0 + c0 + j);
-              atomicAdd(p.out_acc + (size_t)(a / p.k) * p.H + h, __ldg(p.topk_w + a) * __uint_as_float(v[j]));
-            }
+            const int a = __shfl_sync(0xffffffffu, a_l, j);
+            const float w = __shfl_sync(0xffffffffu, w_l, j);
+            if (c0 + j < nrows)
+              atomicAdd(p.out_acc + (size_t)(a / p.k) * p.H + h, w * __uint_as_float(v[j]));
           }
         }
       }
       if (!ok) break;
       tc_fence_before();
-      mbar_arrive(&tmem_empty[b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[b]);
     }
   }
   tc_fence_before();
@@ -613,8 +679,8 @@ static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
 
 bool prefill_fits(int H, int I, int bs, bool has_zp_gu, bool has_zp_d, bool split) {
   if (H % 128 || I % 64 || bs < 32 || (bs & (bs - 1))) return false;
-  int a, b;
-  return gemm_plan(kModeGU, split, H / bs, has_zp_gu, a, b) && gemm_plan(kModeDN, split, I / bs, has_zp_d, a, b);
+  int a, b, c;
+  return gemm_plan(kModeGU, split, H / bs, has_zp_gu, a, b, c) && gemm_plan(kModeDN, split, I / bs, has_zp_d, a, b, c);
 }
 
 cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int, cudaStream_t st, bool pdl) {
@@ -626,8 +692,8 @@ cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int, c
 template <int MODE, typename TA, typename TS, bool Z, bool SPLIT>
 static cudaError_t launch_gemm_t(PrefillParams p, const CUtensorMap* m, cudaStream_t st, bool pdl) {
   const int K = (MODE == kModeGU) ? p.H : p.I;
-  if (!gemm_plan(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz)) return cudaErrorInvalidValue;
-  const GemmSmem L = gemm_smem(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz);
+  if (!gemm_plan(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz, p.npk)) return cudaErrorInvalidValue;
+  const GemmSmem L = gemm_smem(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz, p.npk);
   auto fn = gemm_kernel<MODE, TA, TS, Z, SPLIT>;
   cudaError_t err = ensure_smem(fn, L.total);
   if (err != cudaSuccess) return err;

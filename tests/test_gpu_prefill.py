@@ -161,3 +161,26 @@ def test_prefill_fast_matches_oracle(wl):
 @pytest.mark.parametrize("name", ["prefill", "stack"])
 def test_prefill_fast_full_size_normwise(name):
     check_prefill(S.WORKLOADS[name], seed=1, sample=12, path=B.PATH_PREFILL_FAST, normwise=True)
+
+
+def test_prefill_repeated_many_tiles_per_cta():
+    """T = 16 at the full layer size gives each persistent CTA several
+    weight tiles in a row, which exercises every ring wrap-around; repeated
+    calls must all match the oracle (an ordering bug in the packed-code
+    ring once corrupted a few rows of random tiles here)."""
+    wl = S.WORKLOADS["verify"]
+    L = S.make_layer(wl, seed=3, device=DEV)
+    ws = B.Workspace(wl.T, wl.H, wl.I, wl.E, wl.k)
+    o, tw, ti = B.qmoe_forward(L, ws=ws, path=B.PATH_PREFILL, return_routing=True)
+    ids = ti.cpu().numpy()
+    ref, ref_ids, _, probs = oracle.qmoe_forward(L)
+    near = check_routing(ids, tw.cpu().numpy(), probs, ref_ids, wl.k)
+    if near.any():
+        ref2, _, _, _ = oracle.qmoe_forward(L, forced_ids=ids, forced_w=tw.cpu().double().numpy())
+        ref[near] = ref2[near]
+    for rep in range(4):
+        o = B.qmoe_forward(L, ws=ws, path=B.PATH_PREFILL)
+        torch.cuda.synchronize()
+        assert_close_layer(o, ref, "verify prefill rep %d" % rep)
+    rc, bits = ws.status()
+    assert rc == 0 and bits == 0
