@@ -64,10 +64,8 @@ int check_route_args(const void* x, const void* router_w, int act_dtype, int T, 
   if (E > kMaxExperts || k > kMaxTopk) return QMOE_ERR_UNSUPPORTED;
   if (!aligned(x, 16) || !aligned(router_w, 2)) return QMOE_ERR_INVALID_ARG;
   if ((long long)T * k > (1LL << 30)) return QMOE_ERR_UNSUPPORTED;
-  // router CTA shared memory: x slice of 8 tokens + per-warp partial logits
-  const int split = route_split(T);
-  const int rps = (((H + split - 1) / split) + 7) & ~7;
-  if ((size_t)4 * (8 * rps + 64 * E) > 200 * 1024) return QMOE_ERR_UNSUPPORTED;
+  // router CTA shared memory: x slice, staged router rows, partial logits
+  if (route_smem_bytes(T, H, E, k) > 200 * 1024) return QMOE_ERR_UNSUPPORTED;
   return QMOE_OK;
 }
 
@@ -84,7 +82,7 @@ int enqueue_route(const Ws& ws, const void* x, const void* router_w, int act_dty
   p.E = E;
   p.k = k;
   p.split = route_split(T);
-  p.rows_per_split = (((H + p.split - 1) / p.split) + 7) & ~7;
+  p.rows_per_split = route_rows_per_split(H);
   p.topk_w = ws.at<float>(ws.L.w);
   p.topk_ids = ws.at<int32_t>(ws.L.ids);
   p.user_w = user_w;

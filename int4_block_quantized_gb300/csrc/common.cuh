@@ -102,6 +102,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Asynchronous 16-byte global -> shared copy (LDGSTS), no register round
+// trip, so a thread can have many in flight; cp_async_wait_all() waits for
+// this thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // --------------------------------------------------- packed fp32 (f32x2)
 // Native paired fp32 operations of sm_100+ (one instruction for two lanes
 // of work, round-to-nearest-even like the scalar ones).

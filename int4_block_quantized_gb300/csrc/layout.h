@@ -28,7 +28,6 @@ constexpr int kCtlNtiles = 2;         // u32 prefill: number of token tiles
 constexpr size_t kCtlBytes = 1024;
 
 // ---- router tiling
-constexpr int kRouteTokens = 8;       // tokens per router CTA (one warp each)
 constexpr int kRouteThreads = 256;
 constexpr int kMaxSplit = 8;          // H-splits (one cluster) for small T
 
@@ -60,12 +59,49 @@ struct WsLayout {
 
 QMOE_HD size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-// H-splits per token tile: a cluster of up to 8 CTAs while there are few
-// tiles (T <= 32), one CTA per tile beyond.
-QMOE_HD int route_split(int T) {
-  const int tiles = (T + kRouteTokens - 1) / kRouteTokens;
-  if (tiles > 4) return 1;
-  return kMaxSplit / (tiles > 2 ? 4 : tiles);
+// Router tiling: one cluster of kMaxSplit CTAs per tile of route_tokens()
+// tokens; CTA s reduces rows [s*rps, (s+1)*rps) of H.  32-token tiles when
+// there are many tokens and few experts (fewer re-reads of the router
+// weight), else 8.  Every warp accumulates 8 tokens over a row subset.
+QMOE_HD int route_split(int) { return kMaxSplit; }
+QMOE_HD int route_tokens(int T, int E) { return (T > 4096 && E <= 64) ? 32 : 8; }
+QMOE_HD int route_rows_per_split(int H) { return (((H + kMaxSplit - 1) / kMaxSplit) + 7) & ~7; }
+// router weight rows staged in shared memory per pass (multiple of 8 rows,
+// <= 32 KB for 8-token tiles, <= 16 KB for 32-token tiles)
+QMOE_HD int route_chunk_rows(int H, int E, int tok) {
+  const int rps = route_rows_per_split(H);
+  int rc = ((tok == 32 ? 16384 : 32768) / (2 * E)) & ~7;
+  if (rc < 8) rc = 8;
+  return rc < rps ? rc : rps;
+}
+// chunks of the parallel counting sort (one thread each): E * chunks <= 8192
+QMOE_HD int route_group_chunks(int E) {
+  const int c = 8192 / E;
+  return c < 128 ? c : 128;
+}
+// the grouping CTA stages up to this many assignment ids in shared memory
+constexpr int kRouteStageIds = 16384;
+// ints of shared memory the grouping CTA uses for A assignments
+QMOE_HD size_t route_group_ints(int A, int E) {
+  const size_t ch = route_group_chunks(E);
+  const size_t L = (A + ch - 1) / ch;
+  return (size_t)E * ch + 2 * kRouteThreads + (A <= kRouteStageIds ? L * (ch + 1) : 0);
+}
+QMOE_HD size_t route_align16(size_t v) { return (v + 15) & ~(size_t)15; }
+// dynamic shared memory of a router CTA: x slice [rps][TOK] fp32, staged
+// rows [rc][E] 16-bit, then one region used first for the raw x rows
+// [TOK][rps+8] 16-bit and later for the partial logits [8/(TOK/8)][TOK][E]
+// fp32; or, in the grouping CTA, the counting-sort arrays
+QMOE_HD size_t route_smem_bytes(int T, int H, int E, int k) {
+  const int tok = route_tokens(T, E);
+  const size_t rps = route_rows_per_split(H);
+  const size_t part = (size_t)4 * (64 / tok) * tok * E;
+  const size_t xraw = (size_t)2 * tok * (rps + 8);
+  const size_t compute = 4 * rps * tok + route_align16((size_t)2 * route_chunk_rows(H, E, tok) * E) +
+                         (part > xraw ? part : xraw);
+  const size_t A = (size_t)T * k;
+  const size_t group = A > 256 ? 4 * route_group_ints((int)A, E) : 0;
+  return compute > group ? compute : group;
 }
 
 QMOE_HD WsLayout ws_layout(int T, int H, int I, int E, int k) {

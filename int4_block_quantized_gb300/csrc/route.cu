@@ -116,246 +116,303 @@ __device__ void group_one_warp(const int32_t* ids, bool ids_global, int A, int E
   }
 }
 
-// All 8 warps of one CTA group A assignments (any size; stable).
-__device__ void group_block(int A, int E, int* smem_i, const RouteParams& p, int tid,
-                           uint32_t* status) {
-  const int warp = tid >> 5, lane = tid & 31;
-  int* cntw = smem_i;                                  // [8 warps][E]
-  int* tot = cntw + (kRouteThreads / 32) * E;         // [256]
-  int* scan = tot + kRouteThreads;                    // [256]
-  for (int i = tid; i < (kRouteThreads / 32) * E; i += kRouteThreads) cntw[i] = 0;
+// The whole CTA groups A assignments (any size) by a stable counting sort:
+// thread c < CH owns the contiguous chunk [c*L, (c+1)*L) of assignments;
+// per-(expert, chunk) counts are scanned in expert-major order, which gives
+// each chunk its first position inside every expert; the chunks then
+// scatter in order.  Up to kRouteStageIds ids are first staged with
+// coalesced loads in a chunk-transposed layout (element i of chunk c at
+// i*(CH+1) + c: conflict-free both ways).
+__device__ void group_chunked(int A, int E, int* smem_i, const RouteParams& p, int tid, uint32_t* status) {
+  const int CH = route_group_chunks(E);
+  const int L = (A + CH - 1) / CH;
+  int* cnt = smem_i;                   // [E][CH]
+  int* tsum = cnt + E * CH;            // [256]
+  int* flag = tsum + kRouteThreads;    // [256]
+  int* sids = flag + kRouteThreads;    // [L][CH + 1] when staged
+  const bool staged = A <= kRouteStageIds;
+  if (staged)
+    for (int a = tid; a < A; a += kRouteThreads) sids[(a % L) * (CH + 1) + a / L] = __ldcg(p.topk_ids + a);
+  for (int i = tid; i < E * CH; i += kRouteThreads) cnt[i] = 0;
   __syncthreads();
-  const int slab = (A + 7) / 8;
-  const int a_beg = warp * slab, a_end = min(A, a_beg + slab);
-  for (int base = a_beg; base < a_end; base += 32) {
-    const int a = base + lane;
-    const bool valid = a < a_end;
-    int id = valid ? __ldcg(p.topk_ids + a) : -1;
-    if (valid && (id < 0 || id >= E)) {
+  const int a0 = tid * L, a1 = tid < CH ? min(A, a0 + L) : a0;
+  auto id_of = [&](int a) { return staged ? sids[(a - a0) * (CH + 1) + tid] : __ldcg(p.topk_ids + a); };
+  for (int a = a0; a < a1; ++a) {
+    const int id = id_of(a);
+    if (id < 0 || id >= E)
       set_status(status, QMOE_ST_INDEX);
-      id = -1;
-    }
-    const uint32_t mask = __match_any_sync(0xffffffffu, id);
-    if (id >= 0 && lane == __ffs(mask) - 1) cntw[warp * E + id] += __popc(mask);
-    __syncwarp();
+    else
+      cnt[id * CH + tid] += 1;
   }
   __syncthreads();
-  if (tid < E) {
-    int r = 0;
-    for (int w = 0; w < kRouteThreads / 32; ++w) {
-      const int c = cntw[w * E + tid];
-      cntw[w * E + tid] = r;
-      r += c;
-    }
-    tot[tid] = r;
-  } else {
-    tot[tid] = 0;
-  }
-  scan[tid] = tot[tid];
+  // exclusive scan over the flattened [E][CH] counts
+  const int ntot = E * CH;
+  const int seg = (ntot + kRouteThreads - 1) / kRouteThreads;
+  const int s0 = min(ntot, tid * seg), s1 = min(ntot, s0 + seg);
+  int local = 0;
+  for (int i = s0; i < s1; ++i) local += cnt[i];
+  tsum[tid] = local;
   __syncthreads();
   for (int o = 1; o < kRouteThreads; o <<= 1) {
-    const int v = (tid >= o) ? scan[tid - o] : 0;
+    const int v = tid >= o ? tsum[tid - o] : 0;
     __syncthreads();
-    scan[tid] += v;
+    tsum[tid] += v;
     __syncthreads();
   }
-  const int excl = scan[tid] - tot[tid];
+  int run = tsum[tid] - local;
+  for (int i = s0; i < s1; ++i) {
+    const int c = cnt[i];
+    cnt[i] = run;
+    run += c;
+  }
+  const int total = tsum[kRouteThreads - 1];
+  __syncthreads();
+  // expert offsets and the list of experts with at least one assignment
+  int present = 0;
   if (tid < E) {
-    p.offsets[tid] = excl;
-    if (p.user_offsets) p.user_offsets[tid] = excl;
-    for (int w = 0; w < kRouteThreads / 32; ++w) cntw[w * E + tid] += excl;
+    const int off = cnt[tid * CH];
+    const int next = tid + 1 < E ? cnt[(tid + 1) * CH] : total;
+    p.offsets[tid] = off;
+    if (p.user_offsets) p.user_offsets[tid] = off;
+    present = next > off;
   }
   if (tid == 0) {
-    p.offsets[E] = A;
-    if (p.user_offsets) p.user_offsets[E] = A;
+    p.offsets[E] = total;
+    if (p.user_offsets) p.user_offsets[E] = total;
   }
-  __syncthreads();
-  scan[tid] = (tid < E && tot[tid] > 0) ? 1 : 0;
+  flag[tid] = present;
   __syncthreads();
   for (int o = 1; o < kRouteThreads; o <<= 1) {
-    const int v = (tid >= o) ? scan[tid - o] : 0;
+    const int v = tid >= o ? flag[tid - o] : 0;
     __syncthreads();
-    scan[tid] += v;
+    flag[tid] += v;
     __syncthreads();
   }
-  if (tid < E && tot[tid] > 0) p.active[scan[tid]] = tid;  // slot 1 + exclusive rank
-  if (tid == kRouteThreads - 1) p.active[0] = scan[tid];
-  for (int base = a_beg; base < a_end; base += 32) {
-    const int a = base + lane;
-    const bool valid = a < a_end;
-    int id = valid ? __ldcg(p.topk_ids + a) : -1;
-    if (id >= E) id = -1;
-    const uint32_t mask = __match_any_sync(0xffffffffu, id);
-    if (id >= 0) {
-      const int pos = cntw[warp * E + id] + __popc(mask & ((1u << lane) - 1u));
-      p.perm[pos] = a;
-      if (p.user_perm) p.user_perm[pos] = a;
-    }
-    __syncwarp();
-    if (id >= 0 && lane == __ffs(mask) - 1) cntw[warp * E + id] += __popc(mask);
-    __syncwarp();
+  if (present) p.active[flag[tid]] = tid;  // slot 1 + exclusive rank
+  if (tid == kRouteThreads - 1) p.active[0] = flag[tid];
+  // scatter, each chunk in assignment order
+  for (int a = a0; a < a1; ++a) {
+    const int id = id_of(a);
+    if (id < 0 || id >= E) continue;
+    const int pos = cnt[id * CH + tid]++;
+    p.perm[pos] = a;
+    if (p.user_perm) p.user_perm[pos] = a;
   }
 }
 
-// CLUSTER: gridDim.x H-splits form one cluster per token tile.
-template <typename TA, int ME, bool CLUSTER>
+// One thread-block cluster of kMaxSplit CTAs per tile of TOK tokens.  CTA s
+// owns rows [s*rps, (s+1)*rps) of H.  The raw x rows and the router rows are
+// copied into shared memory with cp.async (all 16-byte pieces in flight at
+// once), x is transposed to [row][token] fp32, and each warp accumulates 8
+// tokens over every NRG-th row (NRG = 8 / (TOK / 8)) in fp32.  The row
+// groups are summed in a fixed order, then, after a cluster barrier, CTA s
+// sums the 8 CTAs' partial logits of its own TOK/8 tokens in rank order
+// (distributed shared memory; deterministic) and runs softmax + top-k, one
+// warp per token.
+template <typename TA, int ME, int TOK>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
+  constexpr int NW = kRouteThreads / 32;
+  constexpr int NTG = TOK / 8;   // token groups of 8
+  constexpr int NRG = NW / NTG;  // row groups
+  constexpr int TPC = TOK / NW;  // tokens per CTA in the softmax phase
   extern __shared__ __align__(16) float smem_f[];
   pdl_wait();  // x may be the previous kernel's output
   pdl_trigger();
-  const int split = blockIdx.x;
-  const int tile = blockIdx.y;
-  const int tiles = gridDim.y;
-  const int t0 = tile * kRouteTokens;
-  const int nt = min(kRouteTokens, p.T - t0);
+  const uint32_t rank = cluster_ctarank();
+  const int t0 = blockIdx.y * TOK;
+  const int nt = min(TOK, p.T - t0);
   const int E = p.E, H = p.H, k = p.k;
   const int rps = p.rows_per_split;
-  const int h0 = split * rps;
+  const int h0 = (int)rank * rps;
   const int rows = max(0, min(H, h0 + rps) - h0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rg = warp % NRG, tg = warp / NRG;
   uint32_t* status = p.ctl + kCtlStatus;
 
-  float* xs = smem_f;                                // [8][rps]
-  float* red = smem_f + kRouteTokens * rps;          // [8 warps][8 tokens][E]
+  const int rc = route_chunk_rows(H, E, TOK);
+  float* xs = smem_f;                                               // [rps][TOK]
+  uint16_t* wch = reinterpret_cast<uint16_t*>(xs + (size_t)rps * TOK);  // [rc][E]
+  float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(wch) + route_align16((size_t)2 * rc * E));
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(part);              // [TOK][rps + 8], before the partials
+  const int xstride = rps + 8;
   __shared__ int sh_last;
-  __shared__ int s_ids[kRouteTokens * kMaxTopk];
 
   const uint16_t* x = static_cast<const uint16_t*>(p.x);
   const uint16_t* rw = static_cast<const uint16_t*>(p.router_w);
+  // rows start on 8-row boundaries, so with 16-byte-aligned bases every
+  // 16-byte piece of a chunk or an x row stays aligned
+  const bool vecw = (reinterpret_cast<uintptr_t>(rw) & 15) == 0;
+  const bool vecx = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (H & 7) == 0;
 
-  for (int i = tid; i < kRouteTokens * rows; i += kRouteThreads) {
-    const int t = i / rows, h = i - t * rows;
-    xs[t * rps + h] = (t < nt) ? Half<TA>::to_float(x[(size_t)(t0 + t) * H + h0 + h]) : 0.f;
+  auto stage_rows = [&](int r0, int nr) {
+    const uint16_t* src = rw + (size_t)(h0 + r0) * E;
+    const int nel = nr * E;
+    if (vecw) {
+      const int n16 = nel >> 3;
+      for (int i = tid; i < n16; i += kRouteThreads) cp_async16(wch + 8 * i, src + 8 * i);
+      for (int i = (n16 << 3) + tid; i < nel; i += kRouteThreads) wch[i] = __ldg(src + i);
+    } else {
+      for (int i = tid; i < nel; i += kRouteThreads) wch[i] = __ldg(src + i);
+    }
+  };
+
+  // ---- raw x rows and the first router chunk, all in flight together
+  if (vecx) {
+    const int n16 = rows >> 3;  // rows is a multiple of 8 when H is
+    for (int i = tid; i < nt * n16; i += kRouteThreads) {
+      const int t = i / n16, c = i - t * n16;
+      cp_async16(xraw + t * xstride + 8 * c, x + (size_t)(t0 + t) * H + h0 + 8 * c);
+    }
+  } else {
+    for (int i = tid; i < nt * rows; i += kRouteThreads) {
+      const int t = i / rows, h = i - t * rows;
+      xraw[t * xstride + h] = x[(size_t)(t0 + t) * H + h0 + h];
+    }
   }
+  stage_rows(0, min(rc, rows));
+  cp_async_wait_all();
   __syncthreads();
-
-  // ---- partial logits over this CTA's rows, fp32 accumulate
-  float acc[kRouteTokens][ME];
-#pragma unroll
-  for (int t = 0; t < kRouteTokens; ++t)
-#pragma unroll
-    for (int m = 0; m < ME; ++m) acc[t][m] = 0.f;
-#pragma unroll 8
-  for (int h = warp; h < rows; h += kRouteThreads / 32) {
-    const uint16_t* row = rw + (size_t)(h0 + h) * E;
-    float wv[ME];
-#pragma unroll
-    for (int m = 0; m < ME; ++m) {
-      const int e = lane + 32 * m;
-      wv[m] = (e < E) ? Half<TA>::to_float(__ldg(row + e)) : 0.f;
-    }
-#pragma unroll
-    for (int t = 0; t < kRouteTokens; ++t) {
-      const float xv = xs[t * rps + h];
-#pragma unroll
-      for (int m = 0; m < ME; ++m) acc[t][m] = fmaf(xv, wv[m], acc[t][m]);
-    }
+  for (int i = tid; i < rows * TOK; i += kRouteThreads) {
+    const int h = i / TOK, t = i % TOK;
+    xs[i] = t < nt ? Half<TA>::to_float(xraw[t * xstride + h]) : 0.f;
   }
-#pragma unroll
-  for (int t = 0; t < kRouteTokens; ++t)
-#pragma unroll
-    for (int m = 0; m < ME; ++m) {
-      const int e = lane + 32 * m;
-      if (e < E) red[(warp * kRouteTokens + t) * E + e] = acc[t][m];
-    }
-  __syncthreads();
+  __syncthreads();  // xs complete; the raw x region is free for the partials
 
-  // ---- combine the 8 warps in a fixed order (into red[0 .. 8E))
-  const int nlog = kRouteTokens * E;
-  for (int i = tid; i < nlog; i += kRouteThreads) {
-    float v = 0.f;
+  // ---- partial logits: 8 tokens per warp over every NRG-th row
+  float acc[8][ME];
 #pragma unroll
-    for (int w = 0; w < kRouteThreads / 32; ++w) v += red[w * nlog + i];
-    red[i] = v;
-  }
-
-  if (CLUSTER) {
-    // the cluster's first CTA sums all splits' partials through DSMEM
-    cluster_sync_all();
-    const uint32_t rank = cluster_ctarank();
-    if (rank == 0) {
-      for (int i = tid; i < nlog; i += kRouteThreads) {
-        float v = red[i];
-        for (int r = 1; r < p.split; ++r) v += ld_dsmem_f32(red + i, (uint32_t)r);
-        red[i] = v;
-      }
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int m = 0; m < ME; ++m) acc[j][m] = 0.f;
+  for (int r0 = 0; r0 < rows; r0 += rc) {
+    const int nr = min(rc, rows - r0);
+    if (r0 > 0) {
+      __syncthreads();  // the previous chunk is consumed
+      stage_rows(r0, nr);
+      cp_async_wait_all();
+      __syncthreads();
     }
-    cluster_sync_all();  // peers keep their shared memory until the reads are done
-    if (rank != 0) return;
-  }
-  __syncthreads();
-
-  // ---- softmax + top-k: one warp per token
-  if (warp < nt) {
-    const int t = t0 + warp;
-    float lg[ME];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int m = 0; m < ME; ++m) {
-      const int e = lane + 32 * m;
-      lg[m] = (e < E) ? red[warp * E + e] + (p.bias ? p.bias[e] : 0.f) : -INFINITY;
-      mx = fmaxf(mx, lg[m]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float ex[ME], sum = 0.f;
-#pragma unroll
-    for (int m = 0; m < ME; ++m) {
-      ex[m] = (lane + 32 * m < E) ? expf(lg[m] - mx) : 0.f;
-      sum += ex[m];
-    }
-    sum = warp_sum(sum);
-    float pr[ME];
-#pragma unroll
-    for (int m = 0; m < ME; ++m) pr[m] = ex[m] / sum;
-    uint32_t chosen = 0;
-    for (int j = 0; j < k; ++j) {
-      float bp = -1.f;
-      int bi = 0x7fffffff;
+#pragma unroll 4
+    for (int h = rg; h < nr; h += NRG) {
+      float wv[ME];
 #pragma unroll
       for (int m = 0; m < ME; ++m) {
         const int e = lane + 32 * m;
-        if (e < E && !((chosen >> m) & 1u) && pr[m] > bp) {
-          bp = pr[m];
-          bi = e;
+        wv[m] = (e < E) ? Half<TA>::to_float(wch[h * E + e]) : 0.f;
+      }
+      const float4* xr = reinterpret_cast<const float4*>(xs + (size_t)(r0 + h) * TOK + tg * 8);
+      const float4 xa = xr[0], xb = xr[1];
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int m = 0; m < ME; ++m) acc[j][m] = fmaf(xv[j], wv[m], acc[j][m]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int m = 0; m < ME; ++m) {
+      const int e = lane + 32 * m;
+      if (e < E) part[((size_t)rg * TOK + tg * 8 + j) * E + e] = acc[j][m];
+    }
+  __syncthreads();
+  if (NRG > 1)  // row groups summed in a fixed order
+    for (int i = tid; i < TOK * E; i += kRouteThreads) {
+      float v = part[i];
+#pragma unroll
+      for (int g = 1; g < NRG; ++g) v += part[(size_t)g * TOK * E + i];
+      part[i] = v;
+    }
+  cluster_sync_all();  // every CTA's partials are complete
+
+  // ---- this CTA's tokens: rank-ordered sum of the partials, softmax, top-k
+  if (warp < TPC) {
+    const int tl = (int)rank * TPC + warp;
+    if (tl < nt) {
+      const int t = t0 + tl;
+      float lg[ME];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int m = 0; m < ME; ++m) {
+        const int e = lane + 32 * m;
+        if (e < E) {
+          float pv[kMaxSplit];
+#pragma unroll
+          for (int r = 0; r < kMaxSplit; ++r) pv[r] = ld_dsmem_f32(part + tl * E + e, (uint32_t)r);
+          float v = 0.f;
+#pragma unroll
+          for (int r = 0; r < kMaxSplit; ++r) v += pv[r];
+          lg[m] = v + (p.bias ? p.bias[e] : 0.f);
+        } else {
+          lg[m] = -INFINITY;
         }
+        mx = fmaxf(mx, lg[m]);
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (op > bp || (op == bp && oi < bi)) {
-          bp = op;
-          bi = oi;
-        }
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float ex[ME], sum = 0.f;
+#pragma unroll
+      for (int m = 0; m < ME; ++m) {
+        ex[m] = (lane + 32 * m < E) ? expf(lg[m] - mx) : 0.f;
+        sum += ex[m];
       }
-      if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
-      if (lane == 0) {
-        const size_t a = (size_t)t * k + j;
-        p.topk_ids[a] = bi;
-        p.topk_w[a] = bp;
-        s_ids[warp * k + j] = bi;
-        if (p.user_ids) p.user_ids[a] = bi;
-        if (p.user_w) p.user_w[a] = bp;
+      sum = warp_sum(sum);
+      float pr[ME];
+#pragma unroll
+      for (int m = 0; m < ME; ++m) pr[m] = ex[m] / sum;
+      uint32_t chosen = 0;
+      for (int j = 0; j < k; ++j) {
+        float bp = -1.f;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int m = 0; m < ME; ++m) {
+          const int e = lane + 32 * m;
+          if (e < E && !((chosen >> m) & 1u) && pr[m] > bp) {
+            bp = pr[m];
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (op > bp || (op == bp && oi < bi)) {
+            bp = op;
+            bi = oi;
+          }
+        }
+        if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
+        if (lane == 0) {
+          const size_t a = (size_t)t * k + j;
+          p.topk_ids[a] = bi;
+          p.topk_w[a] = bp;
+          if (p.user_ids) p.user_ids[a] = bi;
+          if (p.user_w) p.user_w[a] = bp;
+        }
       }
     }
   }
+  // peers keep their shared memory until the reads above are done; the
+  // barrier's release/acquire also publishes the top-k writes cluster-wide
+  cluster_sync_all();
 
   const int A = p.T * k;
   int* smem_i = reinterpret_cast<int*>(smem_f);
-  if (tiles == 1) {
-    // this CTA routed every token: group straight from shared memory
-    __syncthreads();
-    if (warp == 0) group_one_warp(s_ids, false, A, E, smem_i, smem_i + E, p, lane, status);
+  if (gridDim.y == 1) {
+    // one cluster routed every token: its first CTA groups them
+    if (rank == 0 && warp == 0) {
+      group_one_warp(p.topk_ids, true, A, E, smem_i, smem_i + E, p, lane, status);
+    }
     return;
   }
 
-  // ---- the last tile to finish groups all assignments by expert
+  // ---- the last CTA to finish groups all assignments by expert
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     const uint32_t ticket = atomicAdd(p.ctl + kCtlGroupTicket, 1u);
-    sh_last = (ticket == (uint32_t)(tiles - 1));
+    sh_last = (ticket == gridDim.x * gridDim.y - 1);
   }
   __syncthreads();
   if (!sh_last) return;
@@ -364,51 +421,45 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   if (A <= 256) {
     if (warp == 0) group_one_warp(p.topk_ids, true, A, E, smem_i, smem_i + E, p, lane, status);
   } else {
-    group_block(A, E, smem_i, p, tid, status);
+    group_chunked(A, E, smem_i, p, tid, status);
   }
 }
 
-template <typename TA, int ME>
+template <typename TA, int ME, int TOK>
 static cudaError_t launch_route_me(const RouteParams& p, cudaStream_t st, bool pdl, size_t smem) {
-  const int tiles = (p.T + kRouteTokens - 1) / kRouteTokens;
-  dim3 grid(p.split, tiles);
-  if (p.split > 1) {
-    auto fn = route_kernel<TA, ME, true>;
-    cudaError_t err = ensure_smem(fn, smem);
-    if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kRouteThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, fn, p);
-  }
-  auto fn = route_kernel<TA, ME, false>;
+  const int tiles = (p.T + TOK - 1) / TOK;
+  auto fn = route_kernel<TA, ME, TOK>;
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(fn, grid, dim3(kRouteThreads), smem, st, pdl, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kMaxSplit, tiles);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kMaxSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 template <typename TA>
 static cudaError_t launch_route_t(const RouteParams& p, cudaStream_t st, bool pdl) {
-  size_t smem = sizeof(float) * ((size_t)kRouteTokens * p.rows_per_split +
-                                 (size_t)(kRouteThreads / 32) * kRouteTokens * p.E);
-  const size_t grp = sizeof(int) * ((size_t)(kRouteThreads / 32) * p.E + 2 * kRouteThreads);
-  if (smem < grp) smem = grp;
+  const size_t smem = route_smem_bytes(p.T, p.H, p.E, p.k);
   const int me = (p.E + 31) / 32;
-  if (me <= 1) return launch_route_me<TA, 1>(p, st, pdl, smem);
-  if (me <= 2) return launch_route_me<TA, 2>(p, st, pdl, smem);
-  if (me <= 4) return launch_route_me<TA, 4>(p, st, pdl, smem);
-  return launch_route_me<TA, 8>(p, st, pdl, smem);
+  if (route_tokens(p.T, p.E) == 32) {
+    if (me <= 1) return launch_route_me<TA, 1, 32>(p, st, pdl, smem);
+    return launch_route_me<TA, 2, 32>(p, st, pdl, smem);
+  }
+  if (me <= 1) return launch_route_me<TA, 1, 8>(p, st, pdl, smem);
+  if (me <= 2) return launch_route_me<TA, 2, 8>(p, st, pdl, smem);
+  if (me <= 4) return launch_route_me<TA, 4, 8>(p, st, pdl, smem);
+  return launch_route_me<TA, 8, 8>(p, st, pdl, smem);
 }
 
 cudaError_t launch_route(const RouteParams& p, int act_dtype, cudaStream_t st, bool pdl) {
