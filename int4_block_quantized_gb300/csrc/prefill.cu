@@ -15,20 +15,18 @@
 // the tensor core's M dimension.  A gate-up tile stacks 64 gate rows over
 // the same 64 up rows, so gate and up land in one TMEM accumulator and the
 // SwiGLU pairs them in the epilogue.  Per CTA (one per SM, persistent):
-//   warp 0  TMA producer: packed int4 tile (128 rows x 64 codes) + the
-//           tile's block scales / zero points + the token tile (bf16/fp16,
-//           128-byte swizzle) into a 4-stage ring;
-//   warp 1  TMEM allocation and the single-thread tcgen05.mma issuer;
-//   warps 2-5  dequantisers: one thread per weight row turns 64 codes into
-//           RN_operand((q - zp) * scale) and writes them in the canonical
-//           128-byte-swizzled K-major layout the MMA descriptor reads;
-//   warps 6-9  epilogue: tcgen05.ld of the accumulator (double-buffered in
-//           TMEM so the next tile's MMAs overlap), SwiGLU or the weighted
+//   a weight producer streams packed int4 tiles (TMA) and each tile's block
+//           scales / zero points (bulk copies) through a deep ring;
+//   a token producer streams token tiles (TMA, 128-byte swizzle);
+//   eight dequantiser warps turn the codes into exact hi + lo operands in
+//           the canonical 128-byte-swizzled K-major layout;
+//   one thread issues tcgen05.mma into a double-buffered TMEM accumulator;
+//   four epilogue warps tcgen05.ld it and apply SwiGLU or the weighted
 //           fp32 scatter-add.
-// The dequantised values are exact integers times the scale, rounded once to
-// the operand type; K is permuted inside every group of 8 (order 0,4,1,5,
-// 2,6,3,7) identically for weights and activations so one LOP3 yields two
-// operands from a 32-bit word of codes.
+// A dequantised weight w = (q - zp) * s enters the MMAs as hi = RN(w) plus
+// lo = w - hi (an exact sum), or as hi alone on the fast path; K is permuted
+// inside every group of 8 (order 0,4,1,5,2,6,3,7) identically for weights
+// and activations so one LOP3 yields two operands from a 32-bit word.
 #include <cuda.h>
 #include <math.h>
 
@@ -232,13 +230,16 @@ constexpr uint32_t kTmemCols = 256;        // two 128-column accumulators
 constexpr uint32_t kSmemLimit = 232448;    // 227 KB per CTA
 constexpr int kDeqWarps = 8;               // two per SM sub-partition: row = warp%4*32+lane, half = K half
 
-// Warp roles (kGemmThreads = 512):
-//   0      token-tile producer (TMA, L2-resident gathered tokens / SwiGLU output)
+// Warp roles (kGemmThreads = 512; warp w issues from SM sub-partition w % 4):
 //   1      TMEM owner and tcgen05.mma issuer
-//   2      weight producer: packed codes (deep ring) and each tile's scales / zero points
-//   3      idle
-//   4-11   dequantisers
+//   5      token-tile producer (TMA, L2-resident gathered tokens / SwiGLU output)
+//   9      weight producer: packed codes (deep ring) and each tile's scales / zero points
+//   0,4,8,2,6,10,3,7  dequantisers (row quadrant = index % 4, K half = index / 4)
+//   11     idle
 //   12-15  epilogue (TMEM lane quadrant = warp % 4)
+// The three issuing roles share sub-partition 1: measured on GB300, a
+// dequantiser sharing a sub-partition with the MMA issuer or a TMA issuer
+// fell 900-1650 cycles behind the others on every 64-wide K chunk.
 // Shared memory: [barriers][scale buffers][operand stages: A hi, A lo, B hi, B lo][packed ring][exchange]
 struct GemmSmem {
   uint32_t a_lo, b_hi, b_lo, stage;  // offsets inside an operand stage, stage size
@@ -388,13 +389,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
+  // dequantiser index of this warp (-1: another role)
+  const int deq = warp == 0 ? 0 : warp == 4 ? 1 : warp == 8 ? 2 : warp == 2 ? 3 : warp == 6 ? 4 : warp == 10 ? 5
+                : warp == 3 ? 6 : warp == 7 ? 7 : -1;
   pdl_wait();  // routing, token tiles and (down) the SwiGLU output come from earlier grids
   pdl_trigger();
   const int NT = (int)__ldcg(p.ctl + kCtlNtiles);
   const int ntile_total = NT * MB;
   const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
 
-  if (warp == 0) {
+  if (warp == 5) {
     // ============================================================ token-tile producer
     if (lane == 0) {
       int it = 0;
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (*s_abort) drain_ring(b_full, nst, it);
     }
-  } else if (warp == 2) {
+  } else if (warp == 9) {
     // ============================================================ weight producer
     if (lane == 0) {
       int ip = 0, tc = 0;
@@ -504,10 +508,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_wait(fin, 0, nullptr);
       }
     }
-  } else if (warp >= 4 && warp < 4 + kDeqWarps) {
+  } else if (deq >= 0) {
     // ============================================================ dequantisers
-    const int r = (warp & 3) * 32 + lane;  // weight row of the tile
-    const int hh = (warp - 4) >> 2;        // which 32 codes of the 64-wide chunk
+    const int r = (deq & 3) * 32 + lane;  // weight row of the tile
+    const int hh = deq >> 2;              // which 32 codes of the 64-wide chunk
     int it = 0;
     Ring rs, rp, rz;
     bool ok = true;
