@@ -30,6 +30,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "QMoE layer tokens/s; decode HBM GB/s and prefill TFLOPS as % of GB300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel, from the ncu captures summarised under profiles/ (None where the
+# kernel version in this tree has not been captured)
+NCU_TRAFFIC = {"decode": 13768704.0, "prefill": 133138432.0, "stack": None}
 POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24}
 DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 60}
 
@@ -272,7 +276,9 @@ def run_ours(a, wl):
     names = KERNELS[dec]
     P = a.pool or POOL[wl.name]
     if stack:
-        P = wl.layers  # the stack itself: every step runs all its layers
+        # every step runs all the stack's layers; --pool (profiling only)
+        # cycles fewer distinct weight sets through them
+        P = min(P, wl.layers)
     layers = [S.make_weights(wl, seed=0, device=dev, layer=l) for l in range(P)]
     if stack:
         xs = [S.make_x(wl, seed=0, device=dev, layer=0)]
@@ -295,7 +301,7 @@ def run_ours(a, wl):
         x_out.copy_(x_in)
         for l in range(wl.layers):
             B.qmoe_rmsnorm(x_out, out=xn)
-            B.qmoe_forward(layers[l], x=xn, out=x_out, ws=ws, accumulate=True)
+            B.qmoe_forward(layers[l % P], x=xn, out=x_out, ws=ws, accumulate=True)
 
     def step(i):
         if stack:
@@ -383,7 +389,7 @@ def run_ours(a, wl):
     else:
         roof = {"bound": "tensor", "achieved": gu_tfs, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": gu_tfs / pk["bf16_tflops"], "other": {"gbs": gu_gbs, "hbm_frac": gu_gbs / pk["hbm_gbs"]}}
-    roof.update({"traffic": None, "peak_source": pk["source"] + (" (copy GB/s)" if roof["bound"] == "hbm"
+    roof.update({"traffic": NCU_TRAFFIC.get(wl.name), "peak_source": pk["source"] + (" (copy GB/s)" if roof["bound"] == "hbm"
                                                                  else " (bf16 burst)"),
                  "kernel": "decode gate-up (+SwiGLU)" if dec else "grouped GEMM gate-up (+SwiGLU), exact hi+lo operands",
                  "bytes_per_launch": wb["gateup"], "flops_per_launch": wb["gateup_flops"], "launch_ms": gu_ms})
