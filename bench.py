@@ -2,7 +2,7 @@
 """Benchmark: INT4 block-quantized MoE FFN layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config decode|tiny|verify|prefill|stack]
+                    [--config decode|tiny|verify|prefill|stack|e128_decode|e128_prefill|e256_decode|e256_prefill]
 
 A step is one pass of the whole layer (router, expert FFNs, weighted
 combine) over one batch of T tokens.  The default workload is the
@@ -33,9 +33,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel, from the ncu captures summarised under profiles/ (None where the
 # kernel version in this tree has not been captured)
-NCU_TRAFFIC = {"decode": 13768704.0, "prefill": 133138432.0, "stack": None}
-POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24}
-DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 60}
+NCU_TRAFFIC = {"decode": 13768704.0, "prefill": 133138432.0}
+POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24,
+        "e128_decode": 24, "e128_prefill": 8, "e256_decode": 24, "e256_prefill": 8}
+DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 60,
+                 "e128_decode": 24000, "e128_prefill": 480, "e256_decode": 24000, "e256_prefill": 480}
 
 
 def parse():

@@ -173,6 +173,25 @@ int qmoe_forward_profiled(const void* x, int act_dtype, const void* router_w,
                           size_t workspace_bytes, void* stream, void* const* events,
                           int n_events);
 
+/* Shared expert of the MoE block ("Qwen MoE BringUp", IR guide section 3,
+ * "Shared Expert"): every token goes through one more SwiGLU expert whose
+ * output, scaled by a sigmoid gate, is added to the block's output:
+ *   out[t] (+)= sigmoid(x[t] . shared_gate_w) * FFN(x[t])
+ * shared_gate_w is a [H] vector in act_dtype.  The expert's weights use the
+ * same INT4 block format as the routed experts with E = 1: gate/up
+ * [1, I, H/2], down [1, H, I/2] (the pages' model keeps this expert in fp16;
+ * here it is quantised like the others).  It runs as the layer with one
+ * expert, top-1, the gate vector as its router and a sigmoid in place of the
+ * softmax, so the whole MoE block is
+ *   qmoe_forward(..., out, accumulate)  then
+ *   qmoe_shared_expert(..., out, accumulate = 1).
+ * Workspace: qmoe_workspace_size(T, H, I, 1, 1).  Same conventions and
+ * errors as qmoe_forward; shared_gate_w NULL -> QMOE_ERR_INVALID_ARG. */
+int qmoe_shared_expert(const void* x, int act_dtype, const void* shared_gate_w, qmoe_qweight gate,
+                       qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T, int H, int I,
+                       int block_size, void* out, int accumulate, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
 /* qmoe_forward without a caller workspace.  An engineering addition with no
  * counterpart in the method's sources: it serves callers that cannot give
  * the library device memory, such as a plain C host program with no device

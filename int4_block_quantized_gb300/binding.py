@@ -67,6 +67,9 @@ def lib():
         L.qmoe_forward_noalloc.restype = i32
         L.qmoe_forward_noalloc.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
             [vp, vp, vp, i32, vp]
+        L.qmoe_shared_expert.restype = i32
+        L.qmoe_shared_expert.argtypes = [vp, i32, vp, QWeight, QWeight, QWeight] + [i32] * 5 + \
+            [vp, i32, vp, sz, vp]
         L.qmoe_dequant.restype = i32
         L.qmoe_dequant.argtypes = [vp, vp, i32, vp, i32, i32, i32, vp, vp]
         L.qmoe_rmsnorm.restype = i32
@@ -172,6 +175,22 @@ def qmoe_forward(layer, x=None, out=None, ws=None, accumulate=False, path=PATH_A
                                int(path), ws.ptr, ws.nbytes, _stream())
     _check(rc, "qmoe_forward")
     return (o, tw, ti) if return_routing else o
+
+
+def qmoe_shared_expert(layer, x=None, out=None, ws=None, accumulate=False):
+    """out (+)= sigmoid(x . shared_gate_w) * FFN(x) for a shared expert dict
+    (make_shared_expert layout: E = 1 weights plus shared_gate_w [H])."""
+    L = layer
+    x = L["x"] if x is None else x
+    T = x.shape[0]
+    H, I, bs = (int(L[n]) for n in ("H", "I", "block_size"))
+    ws = ws or Workspace(T, H, I, 1, 1, device=x.device)
+    o = out if out is not None else torch.empty((T, H), dtype=x.dtype, device=x.device)
+    rc = lib().qmoe_shared_expert(_p(x), _dt(x), _p(L["shared_gate_w"]), _qw(L, "gate"), _qw(L, "up"),
+                                  _qw(L, "down"), _dt(L["gate_s"]), T, H, I, bs, _p(o),
+                                  int(bool(accumulate)), ws.ptr, ws.nbytes, _stream())
+    _check(rc, "qmoe_shared_expert")
+    return o
 
 
 def qmoe_forward_noalloc(layer, x=None, out=None, accumulate=False, return_routing=False):

@@ -72,8 +72,9 @@ int check_route_args(const void* x, const void* router_w, int act_dtype, int T, 
 int enqueue_route(const Ws& ws, const void* x, const void* router_w, int act_dtype,
                   const float* bias, int T, int H, int E, int k, float* user_w,
                   int32_t* user_ids, int32_t* user_offsets, int32_t* user_perm, cudaStream_t st,
-                  bool pdl = true) {
+                  bool pdl = true, int gate_sigmoid = 0) {
   RouteParams p = {};
+  p.gate_sigmoid = gate_sigmoid;
   p.x = x;
   p.router_w = router_w;
   p.bias = bias;
@@ -187,7 +188,8 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
                  qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
                  int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
                  int32_t* topk_ids_out, int accumulate, int path, void* workspace,
-                 size_t workspace_bytes, void* stream, void* const* events, int n_events) {
+                 size_t workspace_bytes, void* stream, void* const* events, int n_events,
+                 int gate_sigmoid = 0) {
   int rc = check_route_args(x, router_w, act_dtype, T, H, E, k);
   if (rc) return rc;
   if (!out || !aligned(out, 16) || !valid_dtype(scale_dtype) || !valid_bs(block_size))
@@ -236,7 +238,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   };
   if ((rc = mark())) return rc;
   rc = enqueue_route(ws, x, router_w, act_dtype, router_bias, T, H, E, k, topk_w_out, topk_ids_out,
-                     nullptr, nullptr, st, pdl);
+                     nullptr, nullptr, st, pdl, gate_sigmoid);
   if (rc || (rc = mark())) return rc;
 
   if (path == QMOE_PATH_PREFILL || path == QMOE_PATH_PREFILL_FAST) {
@@ -336,6 +338,18 @@ int qmoe_forward(const void* x, int act_dtype, const void* router_w, const float
   return qmoe_forward_ex(x, act_dtype, router_w, router_bias, gate, up, down, scale_dtype, T, H, I,
                          E, k, block_size, out, topk_w_out, topk_ids_out, accumulate,
                          QMOE_PATH_AUTO, workspace, workspace_bytes, stream);
+}
+
+int qmoe_shared_expert(const void* x, int act_dtype, const void* shared_gate_w, qmoe_qweight gate,
+                       qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T, int H, int I,
+                       int block_size, void* out, int accumulate, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (!shared_gate_w) return QMOE_ERR_INVALID_ARG;
+  // the layer with one expert, top-1, the gate vector as its [H, 1] router
+  // and a sigmoid in place of the softmax
+  return forward_impl(x, act_dtype, shared_gate_w, nullptr, gate, up, down, scale_dtype, T, H, I, 1, 1,
+                      block_size, out, nullptr, nullptr, accumulate, QMOE_PATH_AUTO, workspace,
+                      workspace_bytes, stream, nullptr, 0, 1);
 }
 
 int qmoe_dequant(const uint8_t* w, const void* scales, int scale_dtype, const uint8_t* zp, int N,

@@ -141,6 +141,7 @@ struct RouteParams {
   int32_t* perm;          // [T*k] workspace
   int32_t* user_perm;
   uint32_t* ctl;          // control block
+  int gate_sigmoid;       // 0: softmax over the E logits; 1: independent sigmoid per logit
 };
 
 // Decode kernel (weights streamed through shared memory by bulk copies).

@@ -263,13 +263,16 @@ __host__ __device__ inline GemmSmem gemm_smem(int mode, bool split, int nb, bool
 // Pipeline plan.  Two tile-scale buffers first (with one, the weight
 // producer cannot start the next tile's codes until the current tile is
 // dequantised), then 3 operand stages if at least 8 packed slots remain,
-// else 2; the packed ring takes the rest (<= 24 slots).
+// else 2; the packed ring takes the rest (<= 24 slots).  Long reductions
+// with small blocks (large whole-K scale buffers) fall back to one scale
+// buffer and as few as 4 packed slots.
 __host__ inline bool gemm_plan(int mode, bool split, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
   for (int sz = 2; sz >= 1; --sz)
     for (int st = 3; st >= 2; --st) {
+      const int pmin = sz == 1 && st == 2 ? 4 : 8;
       int pk = kMaxPk;
-      while (pk >= 8 && gemm_smem(mode, split, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
-      if (pk >= 8) {
+      while (pk >= pmin && gemm_smem(mode, split, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
+      if (pk >= pmin) {
         nst = st;
         nsz = sz;
         npk = pk;

@@ -351,16 +351,22 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      float ex[ME], sum = 0.f;
-#pragma unroll
-      for (int m = 0; m < ME; ++m) {
-        ex[m] = (lane + 32 * m < E) ? expf(lg[m] - mx) : 0.f;
-        sum += ex[m];
-      }
-      sum = warp_sum(sum);
       float pr[ME];
+      if (p.gate_sigmoid) {
+        // gated shared expert: each logit through its own sigmoid
 #pragma unroll
-      for (int m = 0; m < ME; ++m) pr[m] = ex[m] / sum;
+        for (int m = 0; m < ME; ++m) pr[m] = (lane + 32 * m < E) ? 1.f / (1.f + expf(-lg[m])) : 0.f;
+      } else {
+        float ex[ME], sum = 0.f;
+#pragma unroll
+        for (int m = 0; m < ME; ++m) {
+          ex[m] = (lane + 32 * m < E) ? expf(lg[m] - mx) : 0.f;
+          sum += ex[m];
+        }
+        sum = warp_sum(sum);
+#pragma unroll
+        for (int m = 0; m < ME; ++m) pr[m] = ex[m] / sum;
+      }
       uint32_t chosen = 0;
       for (int j = 0; j < k; ++j) {
         float bp = -1.f;

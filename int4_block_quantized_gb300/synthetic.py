@@ -37,7 +37,11 @@ _TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
 _TID = {"x": 0, "router_w": 1, "router_bias": 2,
         "gate_w": 3, "gate_s": 4, "gate_zp": 5,
         "up_w": 6, "up_s": 7, "up_zp": 8,
-        "down_w": 9, "down_s": 10, "down_zp": 11}
+        "down_w": 9, "down_s": 10, "down_zp": 11,
+        "shared_sg": 12,
+        "shared_gate_w": 13, "shared_gate_s": 14, "shared_gate_zp": 15,
+        "shared_up_w": 16, "shared_up_s": 17, "shared_up_zp": 18,
+        "shared_down_w": 19, "shared_down_s": 20, "shared_down_zp": 21}
 
 
 @dataclass(frozen=True)
@@ -74,6 +78,16 @@ WORKLOADS = {
     "prefill": Workload("prefill", 512, 2048, 1408, 60, 4, 128, BF16, BF16, False, -6, zipf_s=1.1),
     # 24-layer residual stack x += layer(RMSNorm(x)), 2048 tokens
     "stack": Workload("stack", 2048, 2048, 1408, 60, 4, 32, BF16, F16, True, -5, layers=24),
+    # larger-E members of the family: 128 experts, top-8, I = 768 and
+    # 256 experts, top-8, I = 512 (H = 2048), decode and prefill batches
+    "e128_decode": Workload("e128_decode", 1, 2048, 768, 128, 8, 32, F16, F16, True, -5),
+    "e128_prefill": Workload("e128_prefill", 512, 2048, 768, 128, 8, 128, BF16, BF16, False, -6),
+    "e256_decode": Workload("e256_decode", 1, 2048, 512, 256, 8, 32, F16, F16, True, -5),
+    "e256_prefill": Workload("e256_prefill", 512, 2048, 512, 256, 8, 128, BF16, BF16, False, -6),
+    # shared expert of the Qwen1.5-MoE-A2.7B block (intermediate 5632 = 4 x 1408),
+    # in the same INT4 block format; E = k = 1 (make_shared_expert)
+    "shared_decode": Workload("shared_decode", 1, 2048, 5632, 1, 1, 32, F16, F16, True, -5),
+    "shared_prefill": Workload("shared_prefill", 512, 2048, 5632, 1, 1, 128, BF16, BF16, False, -6),
 }
 
 
@@ -133,6 +147,26 @@ def make_weights(wl: Workload, seed: int = 0, device="cpu", layer: int = 0) -> d
 def make_layer(wl: Workload, seed: int = 0, device="cpu", layer: int = 0, T: Optional[int] = None) -> dict:
     """Activations plus one layer's weights, as the dict both sides consume."""
     d = make_weights(wl, seed, device, layer)
+    d["x"] = make_x(wl, seed, device, T=T, layer=layer)
+    d["T"] = d["x"].shape[0]
+    return d
+
+
+def make_shared_expert(wl: Workload, seed: int = 0, device="cpu", layer: int = 0,
+                       T: Optional[int] = None) -> dict:
+    """A shared expert: gate vector shared_gate_w [H] (x's dtype, ~N(0, router
+    std)) and one expert's gate/up/down tensors ([1, I, H/2], [1, H, I/2]),
+    plus activations; keys as in make_layer so the same consumers apply."""
+    d = {}
+    g = _gen(device, seed, layer, "shared_sg")
+    sg = torch.randn((wl.H,), generator=g, device=device, dtype=torch.float32) * wl.router_std
+    d["shared_gate_w"] = sg.to(_TORCH_DTYPE[wl.act_dtype])
+    one = wl.with_(E=1)
+    for p, (N, K) in (("gate", (wl.I, wl.H)), ("up", (wl.I, wl.H)), ("down", (wl.H, wl.I))):
+        w, s, zp = _qweight(one, seed, layer, device, "shared_" + p, N, K)
+        d[p + "_w"], d[p + "_s"], d[p + "_zp"] = w, s, zp
+    d.update(H=wl.H, I=wl.I, E=1, k=1, block_size=wl.block_size,
+             act_dtype=wl.act_dtype, scale_dtype=wl.scale_dtype)
     d["x"] = make_x(wl, seed, device, T=T, layer=layer)
     d["T"] = d["x"].shape[0]
     return d

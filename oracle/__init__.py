@@ -52,6 +52,8 @@ def _load(path=None):
         lib.oracle_group_by_expert.argtypes = [vp, i32, i32, i32, vp, vp]
         lib.oracle_qmoe_forward.restype = ctypes.c_int
         lib.oracle_qmoe_forward.argtypes = [vp, i32, vp, vp] + [vp] * 9 + [i32] * 7 + [vp, dp, dp, vp, dp, dp]
+        lib.oracle_shared_expert.restype = ctypes.c_int
+        lib.oracle_shared_expert.argtypes = [vp, i32, vp] + [vp] * 9 + [i32] * 5 + [dp, dp]
         lib.oracle_rmsnorm.restype = None
         lib.oracle_rmsnorm.argtypes = [vp, i32, i32, i32, ctypes.c_double, i32, dp]
         _lib = lib
@@ -215,6 +217,33 @@ def qmoe_forward(layer, forced_ids=None, forced_w=None):
     if rc != 0:
         raise ValueError("oracle_qmoe_forward rejected its arguments")
     return out, ids, w, probs
+
+
+def shared_expert(layer, x=None):
+    """Gated shared expert in fp64.  `layer` holds shared_gate_w [H] (x's
+    dtype), gate_/up_/down_ w, s, zp of a single expert (E = 1), ints H, I,
+    block_size and dtype codes.  Returns (out [T, H] float64, gate [T])."""
+    L = layer
+    x = _np(L["x"] if x is None else x, np.uint16)
+    T = x.shape[0]
+    H, I, bs = (int(L[n]) for n in ("H", "I", "block_size"))
+    arrs = {}
+    for p in ("gate", "up", "down"):
+        arrs[p + "_w"] = _np(L[p + "_w"], np.uint8)
+        arrs[p + "_s"] = _np(L[p + "_s"], np.uint16)
+        arrs[p + "_zp"] = _np(L.get(p + "_zp"), np.uint8)
+    gw = _np(L["shared_gate_w"], np.uint16)
+    out = np.empty((T, H), dtype=np.float64)
+    gate = np.empty(T, dtype=np.float64)
+    rc = _load().oracle_shared_expert(
+        _ptr(x), int(L["act_dtype"]), _ptr(gw),
+        _ptr(arrs["gate_w"]), _ptr(arrs["gate_s"]), _ptr(arrs["gate_zp"]),
+        _ptr(arrs["up_w"]), _ptr(arrs["up_s"]), _ptr(arrs["up_zp"]),
+        _ptr(arrs["down_w"]), _ptr(arrs["down_s"]), _ptr(arrs["down_zp"]),
+        int(L["scale_dtype"]), T, H, I, bs, _dptr(out), _dptr(gate))
+    if rc != 0:
+        raise ValueError("oracle_shared_expert rejected its arguments")
+    return out, gate
 
 
 def rmsnorm(x, x_dtype, T, H, eps=1e-6, round_bf16=False):

@@ -344,6 +344,42 @@ int oracle_qmoe_forward(const uint16_t* x, int x_dtype, const uint16_t* router_w
   return 0;
 }
 
+/* Shared expert of the MoE block ("Qwen MoE BringUp", IR guide section 3,
+ * "Shared Expert": every token goes through one gated SwiGLU expert whose
+ * output, scaled by its gate, is added to the routed output).  Reading: the
+ * gate is sigmoid(x . gate_w) with gate_w a [H] vector in x's dtype, and the
+ * expert's weights use the same INT4 block format as the routed experts
+ * ([1, I, H/2] gate/up, [1, H, I/2] down).
+ *   out[t] = sigmoid(sum_h x[t,h] * gate_w[h]) * FFN(x[t])   (fp64) */
+int oracle_shared_expert(const uint16_t* x, int x_dtype, const uint16_t* shared_gate_w,
+                         const uint8_t* gate_w, const uint16_t* gate_s, const uint8_t* gate_zp,
+                         const uint8_t* up_w, const uint16_t* up_s, const uint8_t* up_zp,
+                         const uint8_t* down_w, const uint16_t* down_s, const uint8_t* down_zp,
+                         int scale_dtype, int T, int H, int I, int block_size, double* out,
+                         double* gate_out) {
+  if (T < 0 || H <= 0 || I <= 0 || block_size <= 0 || !shared_gate_w) return -1;
+  if (H % block_size || I % block_size || H % 2 || I % 2) return -1;
+  or_qw g = {gate_w, gate_s, gate_zp}, u = {up_w, up_s, up_zp}, d = {down_w, down_s, down_zp};
+  double* xrow = (double*)malloc(sizeof(double) * (size_t)H);
+  double* act = (double*)malloc(sizeof(double) * (size_t)I);
+  double* y = (double*)malloc(sizeof(double) * (size_t)H);
+  for (int64_t t = 0; t < T; ++t) {
+    double logit = 0.0;
+    for (int64_t h = 0; h < H; ++h) {
+      xrow[h] = load16(x, t * (int64_t)H + h, x_dtype);
+      logit += xrow[h] * load16(shared_gate_w, h, x_dtype);
+    }
+    const double gate = 1.0 / (1.0 + exp(-logit));
+    if (gate_out) gate_out[t] = gate;
+    expert_ffn(xrow, 0, g, u, d, scale_dtype, H, I, block_size, act, y);
+    for (int64_t h = 0; h < H; ++h) out[t * (int64_t)H + h] = gate * y[h];
+  }
+  free(xrow);
+  free(act);
+  free(y);
+  return 0;
+}
+
 /* ---- RMSNorm (the layer stack's pre-MoE norm) ---------------------------------
  * IR guide, 1. RMSNorm: y = x / sqrt(mean(x^2) + eps), computed in higher
  * precision; the learned per-channel weight is taken as 1 here (synthetic

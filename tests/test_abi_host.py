@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("qmoe_route", "matmul_nbits", "qmoe_forward", "qmoe_forward_ex", "qmoe_dequant",
               "qmoe_rmsnorm", "qmoe_workspace_size", "qmoe_workspace_init", "qmoe_status_string",
-              "qmoe_get_device_status", "qmoe_forward_noalloc"):
+              "qmoe_get_device_status", "qmoe_forward_noalloc", "qmoe_shared_expert"):
         assert n in names, n
 
 
@@ -135,3 +135,9 @@ def test_noalloc_rejects_oversize_shapes_on_the_host(L):
     args = lambda T: (FAKE, 1, FAKE, None, q, q, q, 1, T, 2048, 1408, 60, 4, 128, FAKE, None, None, 0, None)
     assert L.qmoe_forward_noalloc(*args(512)) == 2
     assert L.qmoe_forward_noalloc(*args(0)) == 1
+
+
+def test_shared_expert_requires_gate_vector(L):
+    from int4_block_quantized_gb300.binding import QWeight
+    q = QWeight(FAKE, FAKE, None)
+    assert L.qmoe_shared_expert(FAKE, 0, None, q, q, q, 0, 1, 2048, 5632, 32, FAKE, 0, FAKE, 1 << 30, None) == 1

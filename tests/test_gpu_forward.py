@@ -62,6 +62,9 @@ DECODE_CASES = [
     S.Workload("e256_k8", 16, 256, 128, 256, 8, 32, S.F16, S.BF16, False, -6),
     S.Workload("ragged", 11, 320, 96, 24, 3, 32, S.F16, S.F16, True, -5),
     S.Workload("zipf", 16, 2048, 1408, 60, 4, 128, S.BF16, S.BF16, False, -6, zipf_s=1.1),
+    S.WORKLOADS["e128_decode"],
+    S.WORKLOADS["e256_decode"],
+    S.WORKLOADS["e128_decode"].with_(name="e128_t8", T=8),
 ]
 
 

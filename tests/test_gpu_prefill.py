@@ -95,6 +95,13 @@ def test_prefill_full_size_sampled():
     check_prefill(S.WORKLOADS["prefill"], seed=1, sample=24)
 
 
+@pytest.mark.parametrize("name", ["e128_prefill", "e256_prefill"])
+def test_larger_e_prefill_full_size_sampled(name):
+    """Larger-E family shapes: 128 experts / I = 768 and 256 experts / I = 512,
+    top-8, T = 512 through the grouped GEMM."""
+    check_prefill(S.WORKLOADS[name], seed=4, sample=16)
+
+
 def test_stack_layer_full_size_sampled():
     """One layer of the T = 2048 stack shape (bf16 tokens, fp16 scales, zp)."""
     wl = S.WORKLOADS["stack"]

@@ -414,3 +414,43 @@ def test_planted_mistake_is_caught(oracle, plant, tmp_path):
     with oracle.using_library(lib):
         assert _pins_fail(oracle) > 0, _PLANTS[plant]
     assert _pins_fail(oracle) == 0
+
+
+def _small_shared(seed=0):
+    from int4_block_quantized_gb300 import synthetic as S
+    wl = S.Workload("sh_small", 3, 64, 32, 1, 1, 32, S.F16, S.F16, True, -5)
+    return S.make_shared_expert(wl, seed=seed)
+
+
+def test_shared_expert_zero_gate_is_half_the_expert(oracle):
+    """Gate vector 0: sigmoid(0) = 1/2 exactly, so the shared expert is half
+    the single-expert layer (E = k = 1, whose routing weight is exactly 1)."""
+    import torch
+    L = _small_shared()
+    L["shared_gate_w"] = torch.zeros_like(L["shared_gate_w"])
+    out, gate = oracle.shared_expert(L)
+    assert np.all(gate == 0.5)
+    L1 = dict(L, router_w=torch.zeros(L["H"], 1, dtype=torch.float16), router_bias=None)
+    ref, ids, w, _ = oracle.qmoe_forward(L1)
+    assert np.all(ids == 0) and np.all(w == 1.0)
+    assert np.array_equal(out, 0.5 * ref)
+
+
+def test_shared_expert_saturated_gate(oracle):
+    """A gate logit of +-65536 saturates the sigmoid to exactly 1 or 0 in
+    double: the shared expert is then the whole expert or nothing."""
+    import torch
+    L = _small_shared(seed=1)
+    gw = torch.zeros_like(L["shared_gate_w"])
+    gw[0] = 16384.0
+    L["shared_gate_w"] = gw
+    x = L["x"].clone()
+    x[:, 0] = 4.0
+    L["x"] = x
+    out, gate = oracle.shared_expert(L)
+    L1 = dict(L, router_w=torch.zeros(L["H"], 1, dtype=torch.float16), router_bias=None)
+    ref, _, _, _ = oracle.qmoe_forward(L1)
+    assert np.all(gate == 1.0) and np.array_equal(out, ref)
+    x[:, 0] = -4.0
+    out, gate = oracle.shared_expert(dict(L, x=x))
+    assert np.all(gate == 0.0) and np.all(out == 0.0)
