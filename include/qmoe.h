@@ -141,6 +141,24 @@ int matmul_nbits(const void* x, int act_dtype, const uint8_t* w, const void* sca
                  int scale_dtype, const uint8_t* zp, int M, int N, int K, int block_size, void* y,
                  void* stream);
 
+/* matmul_nbits with an explicit path and a workspace, for any M (MatMulNBits,
+ * IR guide section 2 "Quantization Scheme" for the weight format and the
+ * dequantize-then-matmul definition).  path:
+ *   DECODE        the CUDA-core path above (workspace unused, may be NULL);
+ *   PREFILL       tensor cores (tcgen05) on the exact split of each
+ *                 dequantised weight into bf16/fp16 hi + lo parts, as in the
+ *                 layer's down projection with one expert of weight 1;
+ *   PREFILL_FAST  the same with the weight rounded once to act_dtype;
+ *   AUTO          DECODE for M <= QMOE_DECODE_MAX_TOKENS, else PREFILL.
+ * The tensor-core paths need N % 128 == 0, K % 64 == 0, x, y, scales and
+ * zero points 16-byte aligned and an initialised workspace (qmoe_workspace_init)
+ * of at least qmoe_workspace_size(M, N, K, 1, 1) bytes (QMOE_ERR_WORKSPACE if
+ * smaller); other shapes return QMOE_ERR_UNSUPPORTED.  y is fully written;
+ * x, w, scales and zp are read only.  Stream-ordered. */
+int matmul_nbits_ex(const void* x, int act_dtype, const uint8_t* w, const void* scales,
+                    int scale_dtype, const uint8_t* zp, int M, int N, int K, int block_size,
+                    void* y, int path, void* workspace, size_t workspace_bytes, void* stream);
+
 /* The whole layer: out[T,H] (act_dtype) = sum over the k chosen experts of
  * p * SwiGLU-FFN_e(x).  gate/up are [E, I, H/2] (N = I, K = H), down is
  * [E, H, I/2] (N = H, K = I); all three share scale_dtype and block_size.

@@ -55,6 +55,8 @@ def lib():
         L.qmoe_route.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.matmul_nbits.restype = i32
         L.matmul_nbits.argtypes = [vp, i32, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]
+        L.matmul_nbits_ex.restype = i32
+        L.matmul_nbits_ex.argtypes = [vp, i32, vp, vp, i32, vp, i32, i32, i32, i32, vp, i32, vp, sz, vp]
         L.qmoe_forward.restype = i32
         L.qmoe_forward.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
             [vp, vp, vp, i32, vp, sz, vp]
@@ -146,6 +148,18 @@ def matmul_nbits(x, w, scales, zp, block_size, out=None):
     y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
     _check(lib().matmul_nbits(_p(x), _dt(x), _p(w), _p(scales), _dt(scales), _p(zp), M, N, K,
                               block_size, _p(y), _stream()), "matmul_nbits")
+    return y
+
+
+def matmul_nbits_ex(x, w, scales, zp, block_size, out=None, path=PATH_AUTO, ws=None):
+    """matmul_nbits for any M: tensor cores above the decode token limit."""
+    M, K = x.shape
+    N = w.shape[-2]
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    ws = ws or Workspace(M, N, K, 1, 1, device=x.device)
+    _check(lib().matmul_nbits_ex(_p(x), _dt(x), _p(w), _p(scales), _dt(scales), _p(zp), M, N, K,
+                                 block_size, _p(y), path, ws.ptr, ws.nbytes, _stream()),
+           "matmul_nbits_ex")
     return y
 
 

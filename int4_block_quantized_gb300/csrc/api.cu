@@ -180,6 +180,47 @@ int matmul_nbits(const void* x, int act_dtype, const uint8_t* w, const void* sca
   return QMOE_OK;
 }
 
+int matmul_nbits_ex(const void* x, int act_dtype, const uint8_t* w, const void* scales, int scale_dtype,
+                    const uint8_t* zp, int M, int N, int K, int block_size, void* y, int path, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_PREFILL_FAST) return QMOE_ERR_INVALID_ARG;
+  if (path == QMOE_PATH_DECODE || (path == QMOE_PATH_AUTO && M <= kDecodeMaxTokens))
+    return matmul_nbits(x, act_dtype, w, scales, scale_dtype, zp, M, N, K, block_size, y, stream);
+  if (!x || !y || !valid_dtype(act_dtype) || !valid_dtype(scale_dtype)) return QMOE_ERR_INVALID_ARG;
+  if (!valid_bs(block_size) || M < 1) return QMOE_ERR_INVALID_ARG;
+  qmoe_qweight q{w, scales, zp};
+  int rc = check_qweight(q, N, K, block_size);
+  if (rc) return rc;
+  if (!aligned(x, 16) || !aligned(y, 16)) return QMOE_ERR_INVALID_ARG;
+  if ((long long)M * K > (1LL << 31)) return QMOE_ERR_UNSUPPORTED;
+  // the GEMM's view: one expert with N rows and a K-long reduction, M tokens
+  const WsLayout L = ws_layout(M, N, K, 1, 1);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
+  const bool split = path != QMOE_PATH_PREFILL_FAST;
+  if (!dense_fits(N, K, block_size, zp != nullptr, split) || !aligned(scales, 16) || !aligned(zp, 16))
+    return QMOE_ERR_UNSUPPORTED;
+  if ((rc = check_device())) return rc;
+  Ws ws{L, static_cast<uint8_t*>(workspace)};
+  PrefillParams p = {};
+  p.w[2] = w;
+  p.s[2] = scales;
+  p.z[2] = zp;
+  p.T = M; p.H = N; p.I = K; p.E = 1; p.k = 1; p.bs = block_size;
+  p.lbs = block_size == 32 ? 5 : (block_size == 64 ? 6 : 7);
+  p.offsets = ws.at<int32_t>(L.offsets);
+  p.perm = ws.at<int32_t>(L.perm);
+  p.topk_w = ws.at<float>(L.w);
+  p.act = ws.at<uint16_t>(L.act16);
+  p.act_lo = split ? ws.at<uint16_t>(L.act16lo) : nullptr;
+  p.out_acc = ws.at<float>(L.outacc);
+  p.tiles = ws.at<int32_t>(L.tiles);
+  p.ctl = ws.at<uint32_t>(L.ctl);
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = cuda_status(launch_dense_setup(p, x, st, true)))) return rc;
+  if ((rc = cuda_status(launch_prefill_gemm(p, 1, act_dtype, scale_dtype, split, st, true)))) return rc;
+  return cuda_status(launch_prefill_convert(p, y, act_dtype, st, true));
+}
+
 }  // extern "C"
 
 namespace {

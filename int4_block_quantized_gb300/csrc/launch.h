@@ -47,6 +47,9 @@ bool decode_fits(int mode, int T, int N, int K, int bs, bool has_zp, int k);
 // gate-up with SwiGLU, mode 1 down with the weighted scatter-add), and the
 // final fp32 -> act_dtype conversion (plus residual)
 bool prefill_fits(int H, int I, int bs, bool has_zp_gu, bool has_zp_d, bool split);
+// dense MatMulNBits on the grouped GEMM (down mode, one expert): N outputs, K inputs
+bool dense_fits(int N, int K, int bs, bool has_zp, bool split);
+cudaError_t launch_dense_setup(const PrefillParams& p, const void* x, cudaStream_t st, bool pdl);
 cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int act_dtype, cudaStream_t st,
                                    bool pdl);
 cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype, int scale_dtype, bool split,

@@ -105,6 +105,59 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint16_t* __restrict
   pdl_trigger();
 }
 
+// ---------------------------------------------------------- dense matmul
+// MatMulNBits through the grouped GEMM's down mode: one "expert", token r
+// is assignment r with weight 1.  Here p.T = M rows of x, p.I = K, p.H = N.
+// Writes the trivial routing and token tiles (block 0), x with K permuted in
+// groups of 8 into p.act, zeros into p.act_lo (x is exact in 16 bits) and
+// into the fp32 accumulator.
+__global__ void __launch_bounds__(256) dense_setup_kernel(const uint16_t* __restrict__ x, PrefillParams p) {
+  pdl_wait();
+  const int M = p.T, K = p.I;
+  if (blockIdx.x == 0) {
+    int32_t* perm = const_cast<int32_t*>(p.perm);
+    float* w = const_cast<float*>(p.topk_w);
+    int32_t* off = const_cast<int32_t*>(p.offsets);
+    for (int r = threadIdx.x; r < M; r += blockDim.x) {
+      perm[r] = r;
+      w[r] = 1.f;
+    }
+    const int nt = (M + kBN - 1) / kBN, rows = (M + nt - 1) / nt;
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) {
+      int32_t* d = p.tiles + 4 * i;
+      d[0] = 0;
+      d[1] = i * rows;
+      d[2] = min(rows, M - i * rows);
+      d[3] = 0;
+    }
+    if (threadIdx.x == 0) {
+      off[0] = 0;
+      off[1] = M;
+      p.ctl[kCtlNtiles] = (uint32_t)nt;
+    }
+  }
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t t0 = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t ng = (size_t)M * (K / 8);
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  uint4* dst = reinterpret_cast<uint4*>(p.act);
+  uint4* dlo = reinterpret_cast<uint4*>(p.act_lo);
+  for (size_t i = t0; i < ng; i += stride) {
+    const uint4 v = __ldg(src + i);
+    uint4 o;  // (e0,e1,..,e7) -> (e0,e4,e1,e5,e2,e6,e3,e7)
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    dst[i] = o;
+    if (dlo) dlo[i] = make_uint4(0, 0, 0, 0);
+  }
+  float4* acc = reinterpret_cast<float4*>(p.out_acc);
+  const size_t n4 = (size_t)M * p.H / 4;
+  for (size_t i = t0; i < n4; i += stride) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  pdl_trigger();
+}
+
 // ---------------------------------------------------------------- convert
 // out = act_dtype(out_acc (+ out if accumulating)), 4 elements per step
 template <typename TA>
@@ -684,6 +737,12 @@ static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool dense_fits(int N, int K, int bs, bool has_zp, bool split) {
+  if (N % 128 || K % 64 || bs < 32 || (bs & (bs - 1))) return false;
+  int a, b, c;
+  return gemm_plan(kModeDN, split, K / bs, has_zp, a, b, c);
+}
+
 bool prefill_fits(int H, int I, int bs, bool has_zp_gu, bool has_zp_d, bool split) {
   if (H % 128 || I % 64 || bs < 32 || (bs & (bs - 1))) return false;
   int a, b, c;
@@ -749,6 +808,13 @@ cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype,
     return cudaErrorNotSupported;
   m[1] = m[0];
   return dispatch_gemm<kModeDN>(p, act_dtype, scale_dtype, p.z[2] != nullptr, split, m, st, pdl);
+}
+
+cudaError_t launch_dense_setup(const PrefillParams& p, const void* x, cudaStream_t st, bool pdl) {
+  const size_t work = (size_t)p.T * (p.I / 8 > p.H / 4 ? p.I / 8 : p.H / 4);
+  const int blocks = (int)((work + 255) / 256 < 1024 ? (work + 255) / 256 : 1024);
+  return launch_kernel(dense_setup_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, st, pdl,
+                       static_cast<const uint16_t*>(x), p);
 }
 
 cudaError_t launch_prefill_convert(const PrefillParams& p, void* out, int act_dtype, cudaStream_t st, bool pdl) {

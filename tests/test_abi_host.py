@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("qmoe_route", "matmul_nbits", "qmoe_forward", "qmoe_forward_ex", "qmoe_dequant",
               "qmoe_rmsnorm", "qmoe_workspace_size", "qmoe_workspace_init", "qmoe_status_string",
-              "qmoe_get_device_status", "qmoe_forward_noalloc", "qmoe_shared_expert"):
+              "qmoe_get_device_status", "qmoe_forward_noalloc", "qmoe_shared_expert",
+              "matmul_nbits_ex"):
         assert n in names, n
 
 
@@ -91,6 +92,26 @@ def test_matmul_nbits_rejects_bad_arguments(L):
     assert call(K=96, bs=64) == 1            # K not a multiple of block_size
     assert call(M=0) == 1
     assert call(w=FAKE + 8) == 1             # packed weights must be 16-byte aligned
+
+
+def test_matmul_nbits_ex_rejects_bad_arguments(L):
+    big = 1 << 40
+    def call(**kw):
+        return L.matmul_nbits_ex(kw.get("x", FAKE), 0, kw.get("w", FAKE), kw.get("s", FAKE), 0, None,
+                                 kw.get("M", 64), kw.get("N", 256), kw.get("K", 512), kw.get("bs", 32),
+                                 kw.get("y", FAKE), kw.get("path", 2), kw.get("ws", FAKE),
+                                 kw.get("wsb", big), None)
+    assert call(path=4) == 1 and call(path=-1) == 1
+    assert call(M=0) == 1
+    assert call(x=None) == 1
+    assert call(K=48) == 1                   # K not a multiple of 32
+    assert call(x=FAKE + 2) == 1             # x must be 16-byte aligned on the tensor-core path
+    assert call(ws=None) == 3
+    assert call(wsb=16) == 3
+    assert call(ws=FAKE + 64) == 3           # workspace not 256-byte aligned
+    assert call(N=200) == 2                  # N not a multiple of 128
+    assert call(K=96) == 2                   # K not a multiple of 64
+    assert call(M=4, path=1, K=48) == 1      # the decode path keeps its own checks
 
 
 def test_forward_rejects_bad_arguments(L):
