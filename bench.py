@@ -33,7 +33,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel, from the ncu captures summarised under profiles/ (None where the
 # kernel version in this tree has not been captured)
-NCU_TRAFFIC = {"decode": 13768704.0, "prefill": 133138432.0}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel from an ncu capture of the current build (None: not yet captured)
+NCU_TRAFFIC = {("prefill", "gateup"): 133138432.0}
 POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24,
         "e128_decode": 24, "e128_prefill": 8, "e256_decode": 24, "e256_prefill": 8}
 DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 60,
@@ -297,7 +299,13 @@ def run_ours(a, wl):
         Ds.append(int(torch.unique(ti).numel()))
     D_mean = sum(Ds) / len(Ds)
     wb = workload_bytes(wl, D_mean)
-    launches_per_step = wl.layers * (len(names) + (1 if stack else 0))
+    # kernels per layer call as the library plans them (1: the fused decode layer)
+    nkern = B.qmoe_forward_kernels(layers[0], wl.T)
+    fused = nkern == 1
+    if fused:
+        names = ["layer"]
+    assert nkern == len(names), (nkern, names)
+    launches_per_step = wl.layers * (nkern + (1 if stack else 0))
 
     def run_stack(x_in, x_out):
         x_out.copy_(x_in)
@@ -358,43 +366,52 @@ def run_ours(a, wl):
     # ---- per-kernel durations for the roofline: events between the kernels
     # (no programmatic overlap), replayed from a CUDA graph so host launch
     # gaps are not measured
-    nk = len(names)
     nrep = 3 if dec else 2
     xprof = [xn.copy_(B.qmoe_rmsnorm(xs[0])) if stack else None]
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(nrep * P)]
-    with torch.cuda.stream(s):
-        for evs in evsets:  # torch creates the CUDA event on first record
-            for ev in evs:
-                ev.record(s)
-    torch.cuda.synchronize(dev)
-    g_prof = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_prof, stream=s):
-        for i, evs in enumerate(evsets):
-            j = i % P
-            if stack:
-                B.qmoe_forward_profiled(layers[j], evs, x=xprof[0], out=outs[0], ws=ws)
-            else:
-                B.qmoe_forward_profiled(layers[j], evs, x=xs[j], out=outs[j], ws=ws)
-    g_prof.replay()
-    torch.cuda.synchronize(dev)
-    g_prof.replay()
-    torch.cuda.synchronize(dev)
-    kms = [statistics.mean(evs[kk].elapsed_time(evs[kk + 1]) for evs in evsets[P:]) for kk in range(nk)]
-    kdict = dict(zip(names, kms))
+
+    def kernel_ms(knames, path):
+        nk = len(knames)
+        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(nrep * P)]
+        with torch.cuda.stream(s):
+            for evs in evsets:  # torch creates the CUDA event on first record
+                for ev in evs:
+                    ev.record(s)
+        torch.cuda.synchronize(dev)
+        g_prof = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_prof, stream=s):
+            for i, evs in enumerate(evsets):
+                j = i % P
+                if stack:
+                    B.qmoe_forward_profiled(layers[j], evs, x=xprof[0], out=outs[0], ws=ws, path=path)
+                else:
+                    B.qmoe_forward_profiled(layers[j], evs, x=xs[j], out=outs[j], ws=ws, path=path)
+        g_prof.replay()
+        torch.cuda.synchronize(dev)
+        g_prof.replay()
+        torch.cuda.synchronize(dev)
+        return dict(zip(knames, [statistics.mean(evs[kk].elapsed_time(evs[kk + 1]) for evs in evsets[P:])
+                                 for kk in range(nk)]))
+
+    kdict = kernel_ms(names, B.PATH_AUTO)
+    # the same layer as three kernels, for the breakdown
+    split_kdict = kernel_ms(KERNELS[True], B.PATH_DECODE_SPLIT) if fused else None
     pk = peaks()
-    gu_ms = kdict["gateup"]
-    gu_gbs = wb["gateup"] / (gu_ms * 1e-3) / 1e9
-    gu_tfs = wb["gateup_flops"] / (gu_ms * 1e-3) / 1e12
-    if dec or wb["gateup"] / pk["hbm_gbs"] / 1e9 >= wb["gateup_flops"] / pk["bf16_tflops"] / 1e12:
+    # dominant kernel: the fused layer, else the gate-up kernel
+    kname, kb, kf = ("layer", wb["layer"], wb["flops"]) if fused else ("gateup", wb["gateup"], wb["gateup_flops"])
+    gu_ms = kdict[kname]
+    gu_gbs = kb / (gu_ms * 1e-3) / 1e9
+    gu_tfs = kf / (gu_ms * 1e-3) / 1e12
+    if dec or kb / pk["hbm_gbs"] / 1e9 >= kf / pk["bf16_tflops"] / 1e12:
         roof = {"bound": "hbm", "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": gu_gbs / pk["hbm_gbs"], "other": {"tflops": gu_tfs, "tensor_frac": gu_tfs / pk["bf16_tflops"]}}
     else:
         roof = {"bound": "tensor", "achieved": gu_tfs, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": gu_tfs / pk["bf16_tflops"], "other": {"gbs": gu_gbs, "hbm_frac": gu_gbs / pk["hbm_gbs"]}}
-    roof.update({"traffic": NCU_TRAFFIC.get(wl.name), "peak_source": pk["source"] + (" (copy GB/s)" if roof["bound"] == "hbm"
-                                                                 else " (bf16 burst)"),
-                 "kernel": "decode gate-up (+SwiGLU)" if dec else "grouped GEMM gate-up (+SwiGLU), exact hi+lo operands",
-                 "bytes_per_launch": wb["gateup"], "flops_per_launch": wb["gateup_flops"], "launch_ms": gu_ms})
+    kdesc = ("fused decode layer (router + gate-up + SwiGLU + down + weighted sum)" if fused
+             else "decode gate-up (+SwiGLU)" if dec else "grouped GEMM gate-up (+SwiGLU), exact hi+lo operands")
+    roof.update({"traffic": NCU_TRAFFIC.get((wl.name, kname)),
+                 "peak_source": pk["source"] + (" (copy GB/s)" if roof["bound"] == "hbm" else " (bf16 burst)"),
+                 "kernel": kdesc, "bytes_per_launch": kb, "flops_per_launch": kf, "launch_ms": gu_ms})
 
     # ---- end to end through the public API: pinned H2D of x, forward, D2H of out
     xh = [x.cpu().pin_memory() for x in xs]
@@ -448,13 +465,13 @@ def run_ours(a, wl):
             "vs_baseline": None, "dtype": "fp16" if wl.act_dtype == 0 else "bf16",
             "data": "synthetic", "config": config_dict(wl, a),
             "roofline": roof,
-            "layer": {"path": "decode" if dec else "prefill (exact hi+lo operands)",
+            "layer": {"path": ("decode, one fused kernel" if fused else "decode") if dec else "prefill (exact hi+lo operands)",
                       "bytes": wb["layer"], "distinct_experts": D_mean, "ms": ms_layer,
                       "hbm_gbs": wb["layer"] / (ms_layer * 1e-3) / 1e9,
                       "hbm_frac": wb["layer"] / (ms_layer * 1e-3) / 1e9 / pk["hbm_gbs"],
                       "tflops": wb["flops"] / (ms_layer * 1e-3) / 1e12,
                       "tensor_frac": wb["flops"] / (ms_layer * 1e-3) / 1e12 / pk["bf16_tflops_sustained"],
-                      "kernel_ms": kdict},
+                      "kernel_ms": kdict, **({"split_path_kernel_ms": split_kdict} if fused else {})},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,

@@ -78,12 +78,18 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
  *                 output rounded once to the activation dtype (bf16/fp16),
  *                 about half the tensor-core work; relative error of order
  *                 2^-9 (bf16) of the magnitude of the summed terms.
+ *   DECODE_SPLIT  DECODE as three kernels (router; gate-up + SwiGLU; down +
+ *                 weighted sum) even where DECODE runs the layer as one
+ *                 cooperative kernel (T <= 4 with gate/up and down either
+ *                 all with or all without zero points).  Same arithmetic,
+ *                 same results bit for bit.
  *   AUTO          DECODE for T <= QMOE_DECODE_MAX_TOKENS, else PREFILL. */
 typedef enum {
   QMOE_PATH_AUTO = 0,
   QMOE_PATH_DECODE = 1,
   QMOE_PATH_PREFILL = 2,
-  QMOE_PATH_PREFILL_FAST = 3
+  QMOE_PATH_PREFILL_FAST = 3,
+  QMOE_PATH_DECODE_SPLIT = 4
 } qmoe_path;
 
 /* One projection for all E experts (see "Packed weights" above). */
@@ -178,6 +184,16 @@ int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const fl
                     int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
                     int32_t* topk_ids_out, int accumulate, int path, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/* Number of kernels one qmoe_forward_ex call with these sizes and this path
+ * launches on the current device: 1 (decode layer fused into one
+ * cooperative kernel), 3 (decode: router, gate-up, down) or 5 (prefill:
+ * router, token permutation, two grouped GEMMs, output conversion).  Host
+ * only, nothing launched.  Negative status (-QMOE_ERR_*) if the arguments
+ * are invalid or the shape is unsupported.  Pointer alignment is not known
+ * here and is assumed to meet the call's rules. */
+int qmoe_forward_kernels(int T, int H, int I, int E, int k, int block_size, int act_dtype,
+                         int scale_dtype, int gate_up_has_zp, int down_has_zp, int path);
 
 /* qmoe_forward_ex for profiling: records events[0] before the first kernel
  * and events[i] after kernel i (router, gate-up, down on the decode path),

@@ -14,7 +14,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmoe.so")
 
 F16, BF16 = 0, 1
-PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_FAST = 0, 1, 2, 3
+PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_FAST, PATH_DECODE_SPLIT = 0, 1, 2, 3, 4
 DECODE_MAX_TOKENS = 16
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported device or shape",
            3: "workspace missing or too small", 4: "CUDA runtime error",
@@ -63,6 +63,8 @@ def lib():
         L.qmoe_forward_ex.restype = i32
         L.qmoe_forward_ex.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
             [vp, vp, vp, i32, i32, vp, sz, vp]
+        L.qmoe_forward_kernels.restype = i32
+        L.qmoe_forward_kernels.argtypes = [i32] * 11
         L.qmoe_forward_profiled.restype = i32
         L.qmoe_forward_profiled.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
             [vp, i32, vp, sz, vp, ctypes.POINTER(ctypes.c_void_p), i32]
@@ -225,6 +227,19 @@ def qmoe_forward_noalloc(layer, x=None, out=None, accumulate=False, return_routi
                                     _stream())
     _check(rc, "qmoe_forward_noalloc")
     return (o, tw, ti) if return_routing else o
+
+
+def qmoe_forward_kernels(layer, T, path=PATH_AUTO):
+    """Kernels one qmoe_forward call on this layer with T tokens launches on
+    the current device (1 fused decode, 3 decode, 5 prefill)."""
+    L = layer
+    H, I, E, k, bs = (int(L[n]) for n in ("H", "I", "E", "k", "block_size"))
+    n = lib().qmoe_forward_kernels(T, H, I, E, k, bs, _dt(L["router_w"]), _dt(L["gate_s"]),
+                                   int(L.get("gate_zp") is not None), int(L.get("down_zp") is not None),
+                                   int(path))
+    if n < 0:
+        _check(-n, "qmoe_forward_kernels")
+    return n
 
 
 def qmoe_forward_profiled(layer, events, x=None, out=None, ws=None, path=PATH_AUTO):

@@ -225,6 +225,15 @@ int matmul_nbits_ex(const void* x, int act_dtype, const uint8_t* w, const void* 
 
 namespace {
 
+// True if the decode layer at these sizes runs as the one cooperative kernel.
+bool fused_fits(int T, int H, int I, int E, int k, int block_size, int act_dtype, int scale_dtype, bool zgu,
+                bool zd) {
+  if (T > kTokGroup || zgu != zd) return false;
+  FusedParams f = {};
+  f.g.T = T; f.g.K = H; f.g.N = I; f.g.E = E; f.g.k = k; f.g.bs = block_size;
+  return launch_fused(f, act_dtype, scale_dtype, zgu, nullptr, false, true) == cudaSuccess;
+}
+
 int forward_impl(const void* x, int act_dtype, const void* router_w, const float* router_bias,
                  qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
                  int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
@@ -239,7 +248,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
       (rc = check_qweight(down, H, I, block_size)))
     return rc;
   if ((gate.zp == nullptr) != (up.zp == nullptr)) return QMOE_ERR_INVALID_ARG;
-  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_PREFILL_FAST) return QMOE_ERR_INVALID_ARG;
+  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_SPLIT) return QMOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(T, H, I, E, k);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
   if ((rc = check_device())) return rc;
@@ -251,6 +260,8 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   const bool pre_ok = prefill_fits(H, I, block_size, zgu, zd, split) && aligned(gate.scales, 16) &&
                       aligned(up.scales, 16) && aligned(down.scales, 16) && aligned(gate.zp, 16) &&
                       aligned(up.zp, 16) && aligned(down.zp, 16);
+  const bool split_decode = path == QMOE_PATH_DECODE_SPLIT;
+  if (split_decode) path = QMOE_PATH_DECODE;
   if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
   if (path == QMOE_PATH_DECODE && !dec_ok) return QMOE_ERR_UNSUPPORTED;
   if ((path == QMOE_PATH_PREFILL || path == QMOE_PATH_PREFILL_FAST) && !pre_ok) return QMOE_ERR_UNSUPPORTED;
@@ -277,6 +288,54 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
     ++ev_i;
     return QMOE_OK;
   };
+  DecodeParams g = {};
+  g.w[0] = gate.w; g.s[0] = gate.scales; g.z[0] = gate.zp;
+  g.w[1] = up.w;   g.s[1] = up.scales;   g.z[1] = up.zp;
+  g.N = I; g.K = H; g.bs = block_size; g.nb = H / block_size;
+  g.E = E; g.k = k; g.T = T;
+  g.active = ws.at<int32_t>(L.active);
+  g.offsets = ws.at<int32_t>(L.offsets);
+  g.perm = ws.at<int32_t>(L.perm);
+  g.topk_w = ws.at<float>(L.w);
+  g.x16 = x;
+  g.act_out = ws.at<float>(L.act);
+  g.act_row_floats = dec_row_floats(I);
+  g.src_row_floats = dec_row_floats(H);
+  g.ctl = ws.at<uint32_t>(L.ctl);
+  DecodeParams d = g;
+  d.w[0] = down.w; d.s[0] = down.scales; d.z[0] = down.zp;
+  d.w[1] = nullptr; d.s[1] = nullptr; d.z[1] = nullptr;
+  d.N = H; d.K = I; d.nb = I / block_size;
+  d.src = ws.at<float>(L.act);
+  d.src_row_floats = dec_row_floats(I);
+  d.x16 = nullptr;
+  d.act_out = nullptr;
+  d.out = out;
+  d.accumulate = accumulate;
+
+  if (path == QMOE_PATH_DECODE && !split_decode &&
+      fused_fits(T, H, I, E, k, block_size, act_dtype, scale_dtype, zgu, zd)) {
+    // the whole layer in one cooperative kernel, if its plan fits
+    FusedParams f = {};
+    f.g = g;
+    f.d = d;
+    f.x = x;
+    f.router_w = router_w;
+    f.bias = router_bias;
+    f.gate_sigmoid = gate_sigmoid;
+    f.rps = route_rows_per_split(H);
+    f.ws_w = ws.at<float>(L.w);
+    f.ws_ids = ws.at<int32_t>(L.ids);
+    f.ws_offsets = ws.at<int32_t>(L.offsets);
+    f.ws_active = ws.at<int32_t>(L.active);
+    f.ws_perm = ws.at<int32_t>(L.perm);
+    f.user_w = topk_w_out;
+    f.user_ids = topk_ids_out;
+    if ((rc = mark())) return rc;
+    if ((rc = cuda_status(launch_fused(f, act_dtype, scale_dtype, zgu, st, pdl, false)))) return rc;
+    return mark();
+  }
+
   if ((rc = mark())) return rc;
   rc = enqueue_route(ws, x, router_w, act_dtype, router_bias, T, H, E, k, topk_w_out, topk_ids_out,
                      nullptr, nullptr, st, pdl, gate_sigmoid);
@@ -313,33 +372,8 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
     return mark();
   }
 
-  DecodeParams g = {};
-  g.w[0] = gate.w; g.s[0] = gate.scales; g.z[0] = gate.zp;
-  g.w[1] = up.w;   g.s[1] = up.scales;   g.z[1] = up.zp;
-  g.N = I; g.K = H; g.bs = block_size; g.nb = H / block_size;
-  g.E = E; g.k = k; g.T = T;
-  g.active = ws.at<int32_t>(L.active);
-  g.offsets = ws.at<int32_t>(L.offsets);
-  g.perm = ws.at<int32_t>(L.perm);
-  g.topk_w = ws.at<float>(L.w);
-  g.x16 = x;
-  g.act_out = ws.at<float>(L.act);
-  g.act_row_floats = dec_row_floats(I);
-  g.src_row_floats = dec_row_floats(H);
-  g.ctl = ws.at<uint32_t>(L.ctl);
   rc = cuda_status(launch_decode(g, kModeGateUp, act_dtype, scale_dtype, zgu, st, pdl));
   if (rc || (rc = mark())) return rc;
-
-  DecodeParams d = g;
-  d.w[0] = down.w; d.s[0] = down.scales; d.z[0] = down.zp;
-  d.w[1] = nullptr; d.s[1] = nullptr; d.z[1] = nullptr;
-  d.N = H; d.K = I; d.nb = I / block_size;
-  d.src = ws.at<float>(L.act);
-  d.src_row_floats = dec_row_floats(I);
-  d.x16 = nullptr;
-  d.act_out = nullptr;
-  d.out = out;
-  d.accumulate = accumulate;
   rc = cuda_status(launch_decode(d, kModeDown, act_dtype, scale_dtype, zd, st, pdl));
   if (rc) return rc;
   return mark();
@@ -357,6 +391,27 @@ int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const fl
   return forward_impl(x, act_dtype, router_w, router_bias, gate, up, down, scale_dtype, T, H, I, E,
                       k, block_size, out, topk_w_out, topk_ids_out, accumulate, path, workspace,
                       workspace_bytes, stream, nullptr, 0);
+}
+
+int qmoe_forward_kernels(int T, int H, int I, int E, int k, int block_size, int act_dtype, int scale_dtype,
+                         int gate_up_has_zp, int down_has_zp, int path) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1 || k > E || E > kMaxExperts || k > kMaxTopk || !valid_dtype(act_dtype) ||
+      !valid_dtype(scale_dtype) || !valid_bs(block_size) || path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_SPLIT)
+    return -QMOE_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc) return -rc;
+  const bool zgu = gate_up_has_zp != 0, zd = down_has_zp != 0;
+  const bool dec_ok = T <= kDecodeMaxTokens && decode_fits(kModeGateUp, T, I, H, block_size, zgu, k) &&
+                      decode_fits(kModeDown, T, H, I, block_size, zd, k);
+  const bool pre_ok = prefill_fits(H, I, block_size, zgu, zd, path != QMOE_PATH_PREFILL_FAST);
+  if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
+  if (path == QMOE_PATH_DECODE || path == QMOE_PATH_DECODE_SPLIT) {
+    if (!dec_ok) return -QMOE_ERR_UNSUPPORTED;
+    if (path == QMOE_PATH_DECODE && fused_fits(T, H, I, E, k, block_size, act_dtype, scale_dtype, zgu, zd))
+      return 1;
+    return 3;
+  }
+  return pre_ok ? 5 : -QMOE_ERR_UNSUPPORTED;
 }
 
 int qmoe_forward_profiled(const void* x, int act_dtype, const void* router_w,

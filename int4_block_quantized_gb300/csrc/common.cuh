@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "layout.h"
@@ -74,15 +75,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the warp is descheduled until the
+// phase completes or about `ns` nanoseconds pass, so waiting warps do not
+// take issue slots from the warps doing the arithmetic.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.b32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: gives up after ~kWaitLimitCycles SM cycles, records
 // QMOE_ST_TIMEOUT in the status word and returns false.  No trap, no hang.
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
-  uint32_t n = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++n & 255u) == 0 && clock64() - t0 > kWaitLimitCycles) {
+  while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
+    if (clock64() - t0 > kWaitLimitCycles) {
       set_status(status, QMOE_ST_TIMEOUT);
       return false;
     }
@@ -229,6 +243,120 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, bool bf16) 
   d |= (uint32_t)(N >> 3) << 17;    // N / 8
   d |= (uint32_t)(M >> 4) << 24;    // M / 16
   return d;
+}
+
+// ----------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// fp32 load from the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t addr = smem_u32(local), raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(addr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------ router top-k
+// One warp, one token: lane holds the logits of experts lane + 32*m (m <
+// ME; -inf beyond E).  Softmax over the E experts (or, for a gated shared
+// expert, an independent sigmoid per logit), then k rounds of arg-max with
+// ties to the lower expert id.  Every lane returns the k ids and raw
+// probabilities.  Both router kernels call this, so they agree bit for bit.
+template <int ME>
+__device__ __forceinline__ void softmax_topk(const float (&lg)[ME], int E, int k, bool gate_sigmoid, int lane,
+                                             int (&ids)[kMaxTopk], float (&wts)[kMaxTopk]) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int m = 0; m < ME; ++m) mx = fmaxf(mx, lg[m]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float pr[ME];
+  if (gate_sigmoid) {
+#pragma unroll
+    for (int m = 0; m < ME; ++m) pr[m] = (lane + 32 * m < E) ? 1.f / (1.f + expf(-lg[m])) : 0.f;
+  } else {
+    float ex[ME], sum = 0.f;
+#pragma unroll
+    for (int m = 0; m < ME; ++m) {
+      ex[m] = (lane + 32 * m < E) ? expf(lg[m] - mx) : 0.f;
+      sum += ex[m];
+    }
+    sum = warp_sum(sum);
+#pragma unroll
+    for (int m = 0; m < ME; ++m) pr[m] = ex[m] / sum;
+  }
+  uint32_t chosen = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) {
+    ids[j] = 0;
+    wts[j] = 0.f;
+  }
+  for (int j = 0; j < k; ++j) {
+    float bp = -1.f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int m = 0; m < ME; ++m) {
+      const int e = lane + 32 * m;
+      if (e < E && !((chosen >> m) & 1u) && pr[m] > bp) {
+        bp = pr[m];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (op > bp || (op == bp && oi < bi)) {
+        bp = op;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
+    // (select, not index: a runtime index would put the arrays in local memory)
+#pragma unroll
+    for (int q = 0; q < kMaxTopk; ++q)
+      if (q == j) {
+        ids[q] = bi;
+        wts[q] = bp;
+      }
+  }
+}
+
+// ------------------------------------------------------- grid barrier
+// One thread per CTA, after a CTA barrier over the threads whose global
+// writes must be published.  ctr[0] counts arrivals, ctr[1] is the
+// generation; the last arrival resets the count and bumps the generation
+// (self-resetting, so the next launch starts clean).  Only valid when all
+// nctas CTAs are co-resident (cooperative launch).  Gives up after
+// ~kWaitLimitCycles: sets QMOE_ST_TIMEOUT and returns false.
+__device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t nctas, uint32_t* status, long long limit) {
+  uint32_t gen;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(ctr + 1) : "memory");
+  __threadfence();
+  const uint32_t old = atomicAdd(ctr, 1u);
+  if (old == nctas - 1) {
+    atomicExch(ctr, 0u);
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ctr + 1), "r"(gen + 1u) : "memory");
+    return true;
+  }
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t g;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(ctr + 1) : "memory");
+    if (g != gen) return true;
+    if (clock64() - t0 > limit) {
+      set_status(status, QMOE_ST_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // ---------------------------------------------- programmatic dependent launch

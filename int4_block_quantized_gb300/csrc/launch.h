@@ -42,6 +42,10 @@ cudaError_t launch_route(const RouteParams& p, int act_dtype, cudaStream_t st, b
 cudaError_t launch_decode(DecodeParams p, int mode, int act_dtype, int scale_dtype, bool has_zp,
                           cudaStream_t st, bool pdl);
 bool decode_fits(int mode, int T, int N, int K, int bs, bool has_zp, int k);
+// fused decode layer (T <= kTokGroup): cudaErrorInvalidValue if the plan
+// does not fit; check_only: plan only, nothing launched
+cudaError_t launch_fused(const FusedParams& f, int act_dtype, int scale_dtype, bool has_zp, cudaStream_t st,
+                         bool pdl, bool check_only);
 
 // prefill path: token gather + tile table, the two grouped GEMMs (mode 0
 // gate-up with SwiGLU, mode 1 down with the weighted scatter-add), and the

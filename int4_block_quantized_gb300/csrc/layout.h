@@ -25,6 +25,8 @@ constexpr int kMaxTopk = 8;
 constexpr int kCtlStatus = 0;         // u32 sticky status bits
 constexpr int kCtlGroupTicket = 1;    // u32 router: token tiles done with top-k
 constexpr int kCtlNtiles = 2;         // u32 prefill: number of token tiles
+constexpr int kCtlGridCount = 3;      // u32 fused decode: grid-barrier arrivals (reset by the last)
+constexpr int kCtlGridGen = 4;        // u32 fused decode: grid-barrier generation
 constexpr size_t kCtlBytes = 1024;
 
 // ---- router tiling
@@ -174,6 +176,24 @@ struct DecodeParams {
   uint32_t slot_base;  // byte offset of the stage ring in shared memory
   int nslots;
   uint32_t* ctl;
+};
+
+// Fused decode layer (router + gate-up + down in one cooperative launch,
+// T <= kTokGroup): the gate-up and down views of the weights plus the router.
+struct FusedParams {
+  DecodeParams g, d;
+  const void* x;          // [T, H] 16-bit
+  const void* router_w;   // [H, E] 16-bit
+  const float* bias;      // [E] or null
+  int gate_sigmoid;
+  int rps;                // router rows per split
+  float* ws_w;            // workspace routing copies (written by CTA 0)
+  int32_t* ws_ids;
+  int32_t* ws_offsets;
+  int32_t* ws_active;
+  int32_t* ws_perm;
+  float* user_w;          // optional user copies of the top-k
+  int32_t* user_ids;
 };
 
 // Prefill path (grouped GEMM on the tensor cores).  The token tile table

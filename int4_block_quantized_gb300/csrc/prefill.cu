@@ -340,15 +340,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
                                               volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  uint32_t n = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++n & 63u) == 0) {
-      if (*abort) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
-        set_status(status, QMOE_ST_TIMEOUT);
-        *abort = 1;
-        return false;
-      }
+  // suspended between checks, so that waiting roles leave the issue slots
+  // to the dequantising warps
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      set_status(status, QMOE_ST_TIMEOUT);
+      *abort = 1;
+      return false;
     }
   }
   return true;

@@ -25,22 +25,6 @@
 
 namespace qmoe {
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  uint32_t addr = smem_u32(local), raddr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(addr), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
-  return v;
-}
-
 // Warp-wide exclusive scan of `v` over lanes.
 __device__ __forceinline__ int warp_excl_scan(int v, int lane) {
   int x = v;
@@ -332,7 +316,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     if (tl < nt) {
       const int t = t0 + tl;
       float lg[ME];
-      float mx = -INFINITY;
 #pragma unroll
       for (int m = 0; m < ME; ++m) {
         const int e = lane + 32 * m;
@@ -347,55 +330,24 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
         } else {
           lg[m] = -INFINITY;
         }
-        mx = fmaxf(mx, lg[m]);
       }
+      int ids[kMaxTopk];
+      float wts[kMaxTopk];
+      softmax_topk<ME>(lg, E, k, p.gate_sigmoid != 0, lane, ids, wts);
+      if (lane < k) {
+        int bi = 0;
+        float bp = 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      float pr[ME];
-      if (p.gate_sigmoid) {
-        // gated shared expert: each logit through its own sigmoid
-#pragma unroll
-        for (int m = 0; m < ME; ++m) pr[m] = (lane + 32 * m < E) ? 1.f / (1.f + expf(-lg[m])) : 0.f;
-      } else {
-        float ex[ME], sum = 0.f;
-#pragma unroll
-        for (int m = 0; m < ME; ++m) {
-          ex[m] = (lane + 32 * m < E) ? expf(lg[m] - mx) : 0.f;
-          sum += ex[m];
-        }
-        sum = warp_sum(sum);
-#pragma unroll
-        for (int m = 0; m < ME; ++m) pr[m] = ex[m] / sum;
-      }
-      uint32_t chosen = 0;
-      for (int j = 0; j < k; ++j) {
-        float bp = -1.f;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int m = 0; m < ME; ++m) {
-          const int e = lane + 32 * m;
-          if (e < E && !((chosen >> m) & 1u) && pr[m] > bp) {
-            bp = pr[m];
-            bi = e;
+        for (int q = 0; q < kMaxTopk; ++q)
+          if (q == lane) {
+            bi = ids[q];
+            bp = wts[q];
           }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (op > bp || (op == bp && oi < bi)) {
-            bp = op;
-            bi = oi;
-          }
-        }
-        if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
-        if (lane == 0) {
-          const size_t a = (size_t)t * k + j;
-          p.topk_ids[a] = bi;
-          p.topk_w[a] = bp;
-          if (p.user_ids) p.user_ids[a] = bi;
-          if (p.user_w) p.user_w[a] = bp;
-        }
+        const size_t a = (size_t)t * k + lane;
+        p.topk_ids[a] = bi;
+        p.topk_w[a] = bp;
+        if (p.user_ids) p.user_ids[a] = bi;
+        if (p.user_w) p.user_w[a] = bp;
       }
     }
   }
