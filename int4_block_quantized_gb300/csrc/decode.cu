@@ -720,6 +720,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) fused_decode_kernel(FusedPa
   uint32_t* status = g.ctl + kCtlStatus;
   const int T = g.T, H = g.K, E = g.E, k = g.k, A = T * k;
   const int NSg = P.g.nslots, NSd = P.d.nslots;
+  // launched in clusters of CL covering the grid, or not at all: every CTA
+  // sees the same values, so all return together before any cluster access
+  if (CL > 1 && (cluster_nctarank() != (uint32_t)CL || cluster_count_x() * CL != gridDim.x)) {
+    if (tid == 0) set_status(g.ctl + kCtlStatus, QMOE_ST_INDEX);
+    return;
+  }
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const int rps = f.rps;
   const int hc0 = (int)rank * VR * rps;
@@ -949,16 +955,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) fused_decode_kernel(FusedPa
 
   if (warp == kCW) {
     // ============================================================ producer
+    // Gate-up bytes first: they are on the critical path to the grid
+    // barrier.  The down weights follow once the gate-up copies in flight
+    // have landed (or, with more stages than slots, once the ring has
+    // turned over), so that they do not share the CTA's HBM bandwidth with
+    // the gate-up stream; they still land while the barrier is pending.
     const int n0g = min(NSg, nsg), n0d = min(NSd, nsd);
     issue_copies<kModeGateUp, HAS_ZP>(g, SLg, P.slot_g, stg, s_perm, ring_g, full_g, NSg, 0, n0g, true, true, lane);
     arrive_range(full_g, NSg, 0, n0g);
-    issue_copies<kModeDown, HAS_ZP>(d, SLd, P.slot_d, std_, s_perm, ring_d, full_d, NSd, 0, n0d, true, false, lane);
     bool ok = true;
+    bool down_w = false;
     int ig = n0g;
     for (; ig < nsg; ++ig) {
       if (!(ok = mbar_wait(&empty_g[ig % NSg], ((ig / NSg) - 1) & 1, status))) break;
+      if (!down_w) {
+        issue_copies<kModeDown, HAS_ZP>(d, SLd, P.slot_d, std_, s_perm, ring_d, full_d, NSd, 0, n0d, true, false, lane);
+        down_w = true;
+      }
       issue_copies<kModeGateUp, HAS_ZP>(g, SLg, P.slot_g, stg, s_perm, ring_g, full_g, NSg, ig, ig + 1, true, true, lane);
       arrive_range(full_g, NSg, ig, ig + 1);
+    }
+    if (!down_w) {
+      if (ok && nsg > 0) ok = mbar_wait(&full_g[(nsg - 1) % NSg], ((nsg - 1) / NSg) & 1, status);
+      issue_copies<kModeDown, HAS_ZP>(d, SLd, P.slot_d, std_, s_perm, ring_d, full_d, NSd, 0, n0d, true, false, lane);
     }
     // down activations: only after the grid barrier (a consumer signals it)
     bool acts = ok && mbar_wait(gbar, 0, status);
