@@ -48,14 +48,14 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="decode", choices=list(POOL))
+    ap.add_argument("--config", default="decode", choices=list(POOL) + ["gptq_repack"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool", type=int, default=None,
                     help="resident weight sets (default: enough that a revisit misses L2); "
                          "smaller pools only for profiler captures, which flush caches themselves")
     a = ap.parse_args()
     if a.steps is None:
-        a.steps = DEFAULT_STEPS[a.config]
+        a.steps = DEFAULT_STEPS.get(a.config, 50)
     if a.warmup is None:
         a.warmup = max(3, min(240, a.steps // 10))
     a.warmup = max(3, a.warmup)
@@ -486,8 +486,56 @@ def run_ours(a, wl):
         dist.destroy_process_group()
 
 
+def run_gptq_repack(a):
+    """One Qwen1.5-MoE-A2.7B layer's GPTQ tensors (gate, up, down of 60
+    experts, bs 32, fp16 scales, qzeros) converted to the canonical layout:
+    bytes read + written per conversion over the CUDA-event time."""
+    import torch
+    from int4_block_quantized_gb300 import binding as B
+    B.lib()
+    E, H, I, bs = 60, 2048, 1408, 32
+    g = torch.Generator(device="cuda").manual_seed(0)
+    mats = []
+    nbytes = 0
+    for K, N in ((H, I), (H, I), (I, H)):
+        qw = torch.randint(0, 2 ** 31 - 1, (E, K // 8, N), generator=g, device="cuda", dtype=torch.int32)
+        qz = torch.randint(0, 2 ** 31 - 1, (E, K // bs, N // 8), generator=g, device="cuda", dtype=torch.int32) & 0x77777777
+        sc = torch.rand((E, K // bs, N), generator=g, device="cuda").to(torch.float16)
+        mats.append((qw, qz, sc))
+        nbytes += 2 * (qw.numel() * 4 + sc.numel() * 2) + qz.numel() * 4 + E * N * (K // bs)
+    steps = a.steps or 50
+    warm = a.warmup if a.warmup is not None else 3
+
+    def step():
+        for qw, qz, sc in mats:
+            B.qmoe_repack_gptq(qw, qz, sc, bs, zero_offset=1)
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    pk = peaks()
+    print(json.dumps({"metric": "GPTQ -> canonical weight repack, GB/s (read + write)", "value": gbs, "unit": "GB/s",
+                      "n_gpus": 1, "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
+                      "dtype": "u32/u16/u8", "data": "synthetic",
+                      "config": {"workload": "GPTQ gate+up+down of one layer: E=60 H=2048 I=1408 bs=32, qzeros, fp16 scales",
+                                 "bytes_per_step": nbytes},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                   "frac": gbs / pk["hbm_gbs"], "traffic": None},
+                      "gpu_launches": 9 * steps}))
+
+
 def main():
     a = parse()
+    if a.config == "gptq_repack":
+        run_gptq_repack(a)
+        return
     from int4_block_quantized_gb300 import synthetic as S
     wl = S.WORKLOADS[a.config]
     if a.impl == "reference":

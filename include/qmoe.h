@@ -263,6 +263,45 @@ int qmoe_dequant(const uint8_t* w, const void* scales, int scale_dtype, const ui
  * rounded to act_dtype.  x and out may alias. */
 int qmoe_rmsnorm(const void* x, void* out, int act_dtype, int T, int H, float eps, void* stream);
 
+/* ---- Weight-format adapters (one-time conversion at model load).
+ *
+ * GPTQ checkpoints into the canonical layout above ("Qwen MoE BringUp",
+ * "Bugs/Issues Found", item 1: GPTQ zero points are stored with an offset
+ * of +1 or +0 depending on the exporter, told apart by the median stored
+ * zero).  Source layout, per expert e (E experts stacked, input-major):
+ *   qweight [E, K/8, N]    int32: bits 4j..4j+3 of word (i, n) = q[8i + j, n]
+ *   qzeros  [E, K/bs, N/8] int32: bits 4j..4j+3 of word (g, i) = stored zero
+ *                          of block g, column 8i + j; or NULL (symmetric
+ *                          int4 without zero points)
+ *   scales  [E, K/bs, N]   16-bit (fp16 or bf16, copied bit for bit)
+ * Output: w_out [E, N, K/2], scales_out [E, N, K/bs], zp_out [E, N, K/bs]
+ * (NULL exactly when qzeros is NULL; the canonical layout then implies
+ * zero point 8).  zp = min(stored + offset, 15): the offset is
+ * *zero_offset_dev when that device pointer is given (for example the
+ * output of qmoe_gptq_zero_offset, read by the kernel, so no host round
+ * trip), else zero_offset (0 or 1).  Requires N a multiple of 8, K a
+ * multiple of 32 and of block_size (32, 64, 128); 4-byte aligned int32
+ * buffers and w_out, 2-byte aligned scales.  Asynchronous on `stream`;
+ * input and output must not overlap.  Bound by HBM (every byte read and
+ * written once). */
+int qmoe_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int E, int K,
+                     int N, int block_size, int zero_offset, const int32_t* zero_offset_dev,
+                     uint8_t* w_out, void* scales_out, uint8_t* zp_out, void* stream);
+
+/* The GPTQ zero-point offset of a qzeros tensor (n_words int32 words, all
+ * experts and projections the caller wants to judge together), written to
+ * the device int *offset_out: 1 if the lower median of the stored zero
+ * points is 7 (the exporter stored zero - 1), else 0.  Asynchronous; pass
+ * offset_out to qmoe_repack_gptq as zero_offset_dev. */
+int qmoe_gptq_zero_offset(const int32_t* qzeros, size_t n_words, int32_t* offset_out, void* stream);
+
+/* Packed 4-bit zero points [rows, ceil(nb/2)] (two per byte, block 2b in
+ * the low nibble, 2b + 1 in the high nibble, each row padded to a byte)
+ * into the canonical one byte per block [rows, nb].  The pages' model
+ * already stores one byte per block; this is the packing ONNX MatMulNBits
+ * uses for 4-bit zero points.  rows = E * N for a stacked projection. */
+int qmoe_unpack_zero_points(const uint8_t* zp_packed, int rows, int nb, uint8_t* zp_out, void* stream);
+
 /* Read (blocking: synchronises `stream`) and clear the device status word
  * of `workspace`.  Returns QMOE_OK, or the first QMOE_ERR_* recorded by a
  * kernel since the last read; *bits_out (may be NULL) gets the raw bits. */

@@ -78,6 +78,12 @@ def lib():
         L.qmoe_dequant.argtypes = [vp, vp, i32, vp, i32, i32, i32, vp, vp]
         L.qmoe_rmsnorm.restype = i32
         L.qmoe_rmsnorm.argtypes = [vp, vp, i32, i32, i32, ctypes.c_float, vp]
+        L.qmoe_repack_gptq.restype = i32
+        L.qmoe_repack_gptq.argtypes = [vp, vp, vp] + [i32] * 5 + [vp, vp, vp, vp, vp]
+        L.qmoe_gptq_zero_offset.restype = i32
+        L.qmoe_gptq_zero_offset.argtypes = [vp, sz, vp, vp]
+        L.qmoe_unpack_zero_points.restype = i32
+        L.qmoe_unpack_zero_points.argtypes = [vp, i32, i32, vp, vp]
         L.qmoe_get_device_status.restype = i32
         L.qmoe_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         _lib = L
@@ -274,3 +280,33 @@ def qmoe_rmsnorm(x, eps=1e-6, out=None):
     o = out if out is not None else torch.empty_like(x)
     _check(lib().qmoe_rmsnorm(_p(x), _p(o), _dt(x), T, H, float(eps), _stream()), "qmoe_rmsnorm")
     return o
+
+
+def qmoe_gptq_zero_offset(qzeros):
+    """Device int32 [1]: 1 if the median stored GPTQ zero point is 7, else 0."""
+    off = torch.empty(1, dtype=torch.int32, device=qzeros.device)
+    _check(lib().qmoe_gptq_zero_offset(_p(qzeros), qzeros.numel(), _p(off), _stream()), "qmoe_gptq_zero_offset")
+    return off
+
+
+def qmoe_repack_gptq(qweight, qzeros, scales, block_size, zero_offset=0, zero_offset_dev=None):
+    """GPTQ (qweight [E, K/8, N] int32, qzeros [E, K/bs, N/8] int32 or None,
+    scales [E, K/bs, N]) -> canonical (w [E, N, K/2] u8, scales [E, N, K/bs],
+    zp [E, N, K/bs] u8 or None)."""
+    E, K8, N = qweight.shape
+    K = 8 * K8
+    nb = K // block_size
+    w = torch.empty((E, N, K // 2), dtype=torch.uint8, device=qweight.device)
+    s = torch.empty((E, N, nb), dtype=scales.dtype, device=qweight.device)
+    zp = torch.empty((E, N, nb), dtype=torch.uint8, device=qweight.device) if qzeros is not None else None
+    _check(lib().qmoe_repack_gptq(_p(qweight), _p(qzeros), _p(scales), E, K, N, block_size, int(zero_offset),
+                                  _p(zero_offset_dev), _p(w), _p(s), _p(zp), _stream()), "qmoe_repack_gptq")
+    return w, s, zp
+
+
+def qmoe_unpack_zero_points(zp_packed, nb):
+    """[rows, ceil(nb/2)] packed zero points -> [rows, nb] uint8."""
+    rows = zp_packed.shape[0]
+    out = torch.empty((rows, nb), dtype=torch.uint8, device=zp_packed.device)
+    _check(lib().qmoe_unpack_zero_points(_p(zp_packed), rows, nb, _p(out), _stream()), "qmoe_unpack_zero_points")
+    return out

@@ -469,6 +469,38 @@ int qmoe_rmsnorm(const void* x, void* out, int act_dtype, int T, int H, float ep
   return cuda_status(launch_rmsnorm(x, out, act_dtype, T, H, eps, (cudaStream_t)stream));
 }
 
+int qmoe_gptq_zero_offset(const int32_t* qzeros, size_t n_words, int32_t* offset_out, void* stream) {
+  if (!qzeros || !offset_out || n_words < 1 || !aligned(qzeros, 4) || !aligned(offset_out, 4))
+    return QMOE_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc) return rc;
+  return cuda_status(launch_gptq_zero_offset(qzeros, n_words, offset_out, (cudaStream_t)stream));
+}
+
+int qmoe_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int E, int K, int N,
+                     int block_size, int zero_offset, const int32_t* zero_offset_dev, uint8_t* w_out,
+                     void* scales_out, uint8_t* zp_out, void* stream) {
+  if (!qweight || !scales || !w_out || !scales_out || (qzeros == nullptr) != (zp_out == nullptr))
+    return QMOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 65535 || N < 8 || N % 8 || K < 32 || K % 32 || !valid_bs(block_size) || K % block_size)
+    return QMOE_ERR_INVALID_ARG;
+  if (zero_offset != 0 && zero_offset != 1) return QMOE_ERR_INVALID_ARG;
+  if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(w_out, 4) || !aligned(scales, 2) ||
+      !aligned(scales_out, 2) || !aligned(zero_offset_dev, 4))
+    return QMOE_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc) return rc;
+  return cuda_status(launch_repack_gptq(qweight, qzeros, scales, E, K, N, block_size, zero_offset, zero_offset_dev,
+                                        w_out, scales_out, zp_out, (cudaStream_t)stream));
+}
+
+int qmoe_unpack_zero_points(const uint8_t* zp_packed, int rows, int nb, uint8_t* zp_out, void* stream) {
+  if (!zp_packed || !zp_out || rows < 1 || nb < 1) return QMOE_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc) return rc;
+  return cuda_status(launch_unpack_zp(zp_packed, zp_out, rows, nb, (cudaStream_t)stream));
+}
+
 int qmoe_get_device_status(void* workspace, uint32_t* bits_out, void* stream) {
   if (!workspace) return QMOE_ERR_WORKSPACE;
   uint32_t bits = 0;

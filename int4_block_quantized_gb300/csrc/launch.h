@@ -42,6 +42,12 @@ cudaError_t launch_route(const RouteParams& p, int act_dtype, cudaStream_t st, b
 cudaError_t launch_decode(DecodeParams p, int mode, int act_dtype, int scale_dtype, bool has_zp,
                           cudaStream_t st, bool pdl);
 bool decode_fits(int mode, int T, int N, int K, int bs, bool has_zp, int k);
+// weight-format adapters (formats.cu)
+cudaError_t launch_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int E, int K,
+                               int N, int bs, int offset, const int32_t* offset_dev, uint8_t* w_out,
+                               void* scales_out, uint8_t* zp_out, cudaStream_t st);
+cudaError_t launch_gptq_zero_offset(const int32_t* qzeros, size_t n_words, int32_t* offset_out, cudaStream_t st);
+cudaError_t launch_unpack_zp(const uint8_t* in, uint8_t* out, int rows, int nb, cudaStream_t st);
 // fused decode layer (T <= kTokGroup): cudaErrorInvalidValue if the plan
 // does not fit; check_only: plan only, nothing launched
 cudaError_t launch_fused(const FusedParams& f, int act_dtype, int scale_dtype, bool has_zp, cudaStream_t st,
