@@ -708,10 +708,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) fused_decode_kernel(FusedPa
   StageEnt* std_ = reinterpret_cast<StageEnt*>(smem + P.std_off);
   uint8_t* ring_g = smem + P.ring_g;
   uint8_t* ring_d = smem + P.ring_d;
-  // router scratch, inside the rings (no copy lands there before routing ends)
+  // router scratch (xs, part, wch) inside the rings: no copy lands there
+  // before routing ends
   float* xs = reinterpret_cast<float*>(smem + P.xs_off);        // [VR*rps][4]
   float* part = reinterpret_cast<float*>(smem + P.part_off);    // [VR][8][4][E]
-  float* vpart = reinterpret_cast<float*>(smem + P.vpart_off);  // [VR][4][E], read by the cluster
+  float* vpart = reinterpret_cast<float*>(smem + P.vpart_off);  // [VR][4][E], read by the cluster (own region)
   uint16_t* wch = reinterpret_cast<uint16_t*>(smem + P.wch_off);  // [pass_rows][E]
 
   const DecodeParams& g = f.g;
@@ -876,9 +877,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) fused_decode_kernel(FusedPa
       }
     }
   }
-  // peers keep their partials until every read above is done
-  if (CL > 1) cluster_sync_all();
-  else __syncthreads();
+  // No second cluster barrier: the split sums peers read sit in a region of
+  // their own that nothing overwrites, and no CTA can exit before the grid
+  // barrier, which every peer reaches only after its reads.
+  __syncthreads();
 
   // grouping by expert (stable), one warp: A <= 32 assignments
   if (warp == 0) {
@@ -1148,9 +1150,11 @@ static bool plan_fused(int T, int H, int I, int E, int k, int bs, bool has_zp, i
   P.res_off = kFFixed;
   const uint32_t xs_b = (uint32_t)VR * rps * 16, part_b = (uint32_t)VR * 8 * 4 * E * 4,
                  vpart_b = (uint32_t)VR * 4 * E * 4;
-  // deepest rings first: down slots, then gate-up slots, then gate-up rows per slot
+  // deepest down ring first; gate-up: the fewest, largest stages first (two
+  // slots of half the CTA's rows streamed faster than four of a quarter),
+  // then more slots, then fewer rows per slot
   for (int nd = nd_max; nd >= 2; --nd)
-  for (int ns = 4; ns >= 2; --ns) {
+  for (int ns = 2; ns <= 4; ++ns) {
     P.d.nslots = nd;
     int sr = (P.g.rows_cta + ns - 1) / ns;
     if (sr > 64) sr = 64;
@@ -1163,7 +1167,9 @@ static bool plan_fused(int T, int H, int I, int E, int k, int bs, bool has_zp, i
       P.slot_g = slot_layout(kModeGateUp, sr, H, H / bs, has_zp, 0, T).bytes;
       P.stg_off = P.res_off + al16(res);
       P.std_off = P.stg_off + 48u * P.g.max_stages;
-      P.ring_g = (P.std_off + 48u * P.d.max_stages + 1023u) & ~1023u;
+      // the split sums peers read: outside the rings, never overwritten
+      P.vpart_off = al16(P.std_off + 48u * P.d.max_stages);
+      P.ring_g = (P.vpart_off + vpart_b + 1023u) & ~1023u;
       P.ring_d = P.ring_g + P.g.nslots * P.slot_g;
       P.smem = P.ring_d + P.d.nslots * P.slot_d;
       if (P.smem > kSmemBudget) continue;
@@ -1171,8 +1177,7 @@ static bool plan_fused(int T, int H, int I, int E, int k, int bs, bool has_zp, i
       const uint32_t room = P.smem - P.ring_g;
       P.xs_off = P.ring_g;
       P.part_off = P.xs_off + al16(xs_b);
-      P.vpart_off = P.part_off + al16(part_b);
-      P.wch_off = P.vpart_off + al16(vpart_b);
+      P.wch_off = P.part_off + al16(part_b);
       const uint32_t used = P.wch_off - P.ring_g;
       if (used >= room) continue;
       int pr = (int)(((room - used) / (2u * E)) & ~7u);
