@@ -342,8 +342,11 @@ __device__ __forceinline__ void softmax_topk(const float (&lg)[ME], int E, int k
 // ------------------------------------------------------- grid barrier
 // One thread per CTA, after a CTA barrier over the threads whose global
 // writes must be published.  ctr[0] counts arrivals, ctr[1] is the
-// generation; the last arrival resets the count and bumps the generation
-// (self-resetting, so the next launch starts clean).  Only valid when all
+// generation.  The last arrival releases the waiters first (a release store
+// of the next generation: every arrival's writes precede its atomic add,
+// and the adds are ordered before the last one) and only then resets the
+// count for the next launch, off the waiters' critical path; the next
+// launch arrives only after this grid has completed.  Only valid when all
 // nctas CTAs are co-resident (cooperative launch).  Gives up after
 // ~kWaitLimitCycles: sets QMOE_ST_TIMEOUT and returns false.
 __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t nctas, uint32_t* status, long long limit) {
@@ -352,9 +355,8 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t nctas, uint
   __threadfence();
   const uint32_t old = atomicAdd(ctr, 1u);
   if (old == nctas - 1) {
-    atomicExch(ctr, 0u);
-    __threadfence();
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ctr + 1), "r"(gen + 1u) : "memory");
+    atomicExch(ctr, 0u);
     return true;
   }
   const long long t0 = clock64();
