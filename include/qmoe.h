@@ -78,18 +78,25 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
  *                 output rounded once to the activation dtype (bf16/fp16),
  *                 about half the tensor-core work; relative error of order
  *                 2^-9 (bf16) of the magnitude of the summed terms.
- *   DECODE_SPLIT  DECODE as three kernels (router; gate-up + SwiGLU; down +
- *                 weighted sum) even where DECODE runs the layer as one
- *                 cooperative kernel (T <= 4 with gate/up and down either
- *                 all with or all without zero points).  Same arithmetic,
- *                 same results bit for bit.
+ *                 At T = 1 (gate/up and down either all with or all
+ *                 without zero points) the whole layer runs as one
+ *                 cooperative kernel; otherwise as three kernels (router;
+ *                 gate-up + SwiGLU; down + weighted sum).
+ *   DECODE_SPLIT  DECODE as three kernels always.
+ *   DECODE_FUSED  DECODE as the one cooperative kernel for T <= 4 (at
+ *                 T = 2..4 three kernels are faster on GB300, so DECODE
+ *                 does not choose it there); QMOE_ERR_UNSUPPORTED if its
+ *                 shared-memory plan does not fit.  The three decode
+ *                 variants compute the same arithmetic in the same order:
+ *                 results equal bit for bit.
  *   AUTO          DECODE for T <= QMOE_DECODE_MAX_TOKENS, else PREFILL. */
 typedef enum {
   QMOE_PATH_AUTO = 0,
   QMOE_PATH_DECODE = 1,
   QMOE_PATH_PREFILL = 2,
   QMOE_PATH_PREFILL_FAST = 3,
-  QMOE_PATH_DECODE_SPLIT = 4
+  QMOE_PATH_DECODE_SPLIT = 4,
+  QMOE_PATH_DECODE_FUSED = 5
 } qmoe_path;
 
 /* One projection for all E experts (see "Packed weights" above). */

@@ -225,7 +225,12 @@ int matmul_nbits_ex(const void* x, int act_dtype, const uint8_t* w, const void* 
 
 namespace {
 
-// True if the decode layer at these sizes runs as the one cooperative kernel.
+// The one-kernel decode layer: the default decode path at T = 1, where it
+// is faster than three kernels; at T = 2..4 three kernels stream the larger
+// weight volume faster (measured on GB300), so there it runs only when
+// asked for (QMOE_PATH_DECODE_FUSED).
+constexpr int kFusedAutoMaxTokens = 1;
+// True if the decode layer at these sizes can run as the one cooperative kernel.
 bool fused_fits(int T, int H, int I, int E, int k, int block_size, int act_dtype, int scale_dtype, bool zgu,
                 bool zd) {
   if (T > kTokGroup || zgu != zd) return false;
@@ -248,7 +253,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
       (rc = check_qweight(down, H, I, block_size)))
     return rc;
   if ((gate.zp == nullptr) != (up.zp == nullptr)) return QMOE_ERR_INVALID_ARG;
-  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_SPLIT) return QMOE_ERR_INVALID_ARG;
+  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_FUSED) return QMOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(T, H, I, E, k);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
   if ((rc = check_device())) return rc;
@@ -261,7 +266,8 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
                       aligned(up.scales, 16) && aligned(down.scales, 16) && aligned(gate.zp, 16) &&
                       aligned(up.zp, 16) && aligned(down.zp, 16);
   const bool split_decode = path == QMOE_PATH_DECODE_SPLIT;
-  if (split_decode) path = QMOE_PATH_DECODE;
+  const bool force_fused = path == QMOE_PATH_DECODE_FUSED;
+  if (split_decode || force_fused) path = QMOE_PATH_DECODE;
   if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
   if (path == QMOE_PATH_DECODE && !dec_ok) return QMOE_ERR_UNSUPPORTED;
   if ((path == QMOE_PATH_PREFILL || path == QMOE_PATH_PREFILL_FAST) && !pre_ok) return QMOE_ERR_UNSUPPORTED;
@@ -313,8 +319,10 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   d.out = out;
   d.accumulate = accumulate;
 
-  if (path == QMOE_PATH_DECODE && !split_decode &&
-      fused_fits(T, H, I, E, k, block_size, act_dtype, scale_dtype, zgu, zd)) {
+  const bool fused = path == QMOE_PATH_DECODE && !split_decode && (force_fused || T <= kFusedAutoMaxTokens) &&
+                     fused_fits(T, H, I, E, k, block_size, act_dtype, scale_dtype, zgu, zd);
+  if (force_fused && !fused) return QMOE_ERR_UNSUPPORTED;
+  if (fused) {
     // the whole layer in one cooperative kernel, if its plan fits
     FusedParams f = {};
     f.g = g;
@@ -396,7 +404,7 @@ int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const fl
 int qmoe_forward_kernels(int T, int H, int I, int E, int k, int block_size, int act_dtype, int scale_dtype,
                          int gate_up_has_zp, int down_has_zp, int path) {
   if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1 || k > E || E > kMaxExperts || k > kMaxTopk || !valid_dtype(act_dtype) ||
-      !valid_dtype(scale_dtype) || !valid_bs(block_size) || path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_SPLIT)
+      !valid_dtype(scale_dtype) || !valid_bs(block_size) || path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_FUSED)
     return -QMOE_ERR_INVALID_ARG;
   int rc = check_device();
   if (rc) return -rc;
@@ -405,10 +413,11 @@ int qmoe_forward_kernels(int T, int H, int I, int E, int k, int block_size, int 
                       decode_fits(kModeDown, T, H, I, block_size, zd, k);
   const bool pre_ok = prefill_fits(H, I, block_size, zgu, zd, path != QMOE_PATH_PREFILL_FAST);
   if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
-  if (path == QMOE_PATH_DECODE || path == QMOE_PATH_DECODE_SPLIT) {
+  if (path == QMOE_PATH_DECODE || path == QMOE_PATH_DECODE_SPLIT || path == QMOE_PATH_DECODE_FUSED) {
     if (!dec_ok) return -QMOE_ERR_UNSUPPORTED;
-    if (path == QMOE_PATH_DECODE && fused_fits(T, H, I, E, k, block_size, act_dtype, scale_dtype, zgu, zd))
-      return 1;
+    const bool fits = fused_fits(T, H, I, E, k, block_size, act_dtype, scale_dtype, zgu, zd);
+    if (path == QMOE_PATH_DECODE_FUSED) return fits ? 1 : -QMOE_ERR_UNSUPPORTED;
+    if (path == QMOE_PATH_DECODE && T <= kFusedAutoMaxTokens && fits) return 1;
     return 3;
   }
   return pre_ok ? 5 : -QMOE_ERR_UNSUPPORTED;

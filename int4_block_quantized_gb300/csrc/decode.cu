@@ -1150,45 +1150,62 @@ static bool plan_fused(int T, int H, int I, int E, int k, int bs, bool has_zp, i
   P.res_off = kFFixed;
   const uint32_t xs_b = (uint32_t)VR * rps * 16, part_b = (uint32_t)VR * 8 * 4 * E * 4,
                  vpart_b = (uint32_t)VR * 4 * E * 4;
-  // deepest down ring first; gate-up: the fewest, largest stages first (two
-  // slots of half the CTA's rows streamed faster than four of a quarter),
-  // then more slots, then fewer rows per slot
+  // Choose the ring shapes that keep the most gate-up rows in flight (the
+  // stream that gates the grid barrier); among equals, fewer and larger
+  // stages (two slots of half the CTA's rows streamed faster than four of
+  // a quarter), then the deeper down ring.
+  FusedPlan best = {};
+  int best_rows = 0, best_ns = 0, best_nd = 0;
   for (int nd = nd_max; nd >= 2; --nd)
-  for (int ns = 2; ns <= 4; ++ns) {
-    P.d.nslots = nd;
-    int sr = (P.g.rows_cta + ns - 1) / ns;
-    if (sr > 64) sr = 64;
-    for (; sr >= 1; sr = sr > 8 ? sr * 3 / 4 : sr - 1) {
-      const int nst_min = (P.g.rows_cta + sr - 1) / sr;
-      P.g.slot_rows = sr;
-      P.g.max_stages = nst_min + (P.g.rows_cta + I - 1) / I + 1;
-      P.g.nslots = ns < P.g.max_stages ? ns : P.g.max_stages;
-      if (P.g.nslots < 2) P.g.nslots = 2;
-      P.slot_g = slot_layout(kModeGateUp, sr, H, H / bs, has_zp, 0, T).bytes;
-      P.stg_off = P.res_off + al16(res);
-      P.std_off = P.stg_off + 48u * P.g.max_stages;
-      // the split sums peers read: outside the rings, never overwritten
-      P.vpart_off = al16(P.std_off + 48u * P.d.max_stages);
-      P.ring_g = (P.vpart_off + vpart_b + 1023u) & ~1023u;
-      P.ring_d = P.ring_g + P.g.nslots * P.slot_g;
-      P.smem = P.ring_d + P.d.nslots * P.slot_d;
-      if (P.smem > kSmemBudget) continue;
-      // router scratch inside the rings
-      const uint32_t room = P.smem - P.ring_g;
-      P.xs_off = P.ring_g;
-      P.part_off = P.xs_off + al16(xs_b);
-      P.wch_off = P.part_off + al16(part_b);
-      const uint32_t used = P.wch_off - P.ring_g;
-      if (used >= room) continue;
-      int pr = (int)(((room - used) / (2u * E)) & ~7u);
-      if (pr > VR * rps) pr = VR * rps;
-      if (pr < 8) continue;
-      P.pass_rows = pr;
-      *out = P;
-      return true;
+    for (int ns = 2; ns <= 4; ++ns) {
+      P.d.nslots = nd;
+      int sr = (P.g.rows_cta + ns - 1) / ns;
+      if (sr > 64) sr = 64;
+      for (; sr >= 1; sr = sr > 8 ? sr * 3 / 4 : sr - 1) {
+        const int nst_min = (P.g.rows_cta + sr - 1) / sr;
+        P.g.slot_rows = sr;
+        P.g.max_stages = nst_min + (P.g.rows_cta + I - 1) / I + 1;
+        P.g.nslots = ns < P.g.max_stages ? ns : P.g.max_stages;
+        if (P.g.nslots < 2) P.g.nslots = 2;
+        P.slot_g = slot_layout(kModeGateUp, sr, H, H / bs, has_zp, 0, T).bytes;
+        P.stg_off = P.res_off + al16(res);
+        P.std_off = P.stg_off + 48u * P.g.max_stages;
+        // the split sums peers read: outside the rings, never overwritten
+        P.vpart_off = al16(P.std_off + 48u * P.d.max_stages);
+        P.ring_g = (P.vpart_off + vpart_b + 1023u) & ~1023u;
+        P.ring_d = P.ring_g + P.g.nslots * P.slot_g;
+        P.smem = P.ring_d + P.d.nslots * P.slot_d;
+        if (P.smem > kSmemBudget) continue;
+        // router scratch inside the rings; small rings (few rows per CTA)
+        // are extended until it fits with at least 8 router rows per pass
+        uint32_t room = P.smem - P.ring_g;
+        P.xs_off = P.ring_g;
+        P.part_off = P.xs_off + al16(xs_b);
+        P.wch_off = P.part_off + al16(part_b);
+        const uint32_t used = P.wch_off - P.ring_g;
+        if (room < used + 16u * E) {
+          room = (used + 16u * E + 127u) & ~127u;
+          P.smem = P.ring_g + room;
+          if (P.smem > kSmemBudget) continue;
+        }
+        int pr = (int)(((room - used) / (2u * E)) & ~7u);
+        if (pr > VR * rps) pr = VR * rps;
+        if (pr < 8) continue;
+        P.pass_rows = pr;
+        const int rows = min(P.g.nslots * sr, P.g.rows_cta);
+        if (rows > best_rows || (rows == best_rows && ns < best_ns)) {
+          best = P;
+          best_rows = rows;
+          best_ns = ns;
+          best_nd = nd;
+        }
+        break;  // the largest slot that fits for this (nd, ns)
+      }
     }
-  }
-  return false;
+  (void)best_nd;
+  if (best_rows == 0) return false;
+  *out = best;
+  return true;
 }
 
 // CTAs of a cooperative launch in clusters of kFusedCluster at one CTA per

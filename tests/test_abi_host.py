@@ -127,7 +127,7 @@ def test_forward_rejects_bad_arguments(L):
     assert call(g=qz) == 1                   # gate and up must agree on zero points
     assert call(I=100) == 1                  # I not a multiple of 32
     assert call(H=256, bs=128, I=64) == 1    # I not a multiple of block_size
-    assert call(path=5) == 1
+    assert call(path=6) == 1
     assert call(out=None) == 1
     assert call(wsb=100) == 3
     assert call(k=3, E=2) == 1

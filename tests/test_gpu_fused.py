@@ -1,6 +1,7 @@
 """The fused decode layer (router, gate-up and down in one cooperative
-kernel, T <= 4) against the three-kernel decode path: the same arithmetic
-in the same order, so outputs and routing must agree bit for bit.  Also the
+kernel, T <= 4; the default decode path at T = 1) against the three-kernel
+decode path: the same arithmetic in the same order, so outputs and routing
+must agree bit for bit.  Also the
 grid barrier over many back-to-back calls (its counter resets itself), the
 residual add, and the shapes that fall back to three kernels."""
 import pytest
@@ -27,7 +28,7 @@ def _both(L, wl, accumulate=False, seed=0):
         base = torch.randn(x.shape, generator=torch.Generator(device=DEV).manual_seed(seed + 5),
                            device=DEV).to(x.dtype)
     res = []
-    for path in (B.PATH_DECODE, B.PATH_DECODE_SPLIT):
+    for path in (B.PATH_DECODE_FUSED, B.PATH_DECODE_SPLIT):
         ws = B.Workspace(x.shape[0], wl.H, wl.I, wl.E, wl.k)
         out = base.clone() if accumulate else None
         o, tw, ti = B.qmoe_forward(L, out=out, ws=ws, accumulate=accumulate, path=path, return_routing=True)
@@ -104,18 +105,28 @@ def test_fused_in_a_cuda_graph():
 
 
 def test_mixed_zero_points_fall_back_and_agree():
+    """Gate/up with zero points and down without: no fused plan.  The forced
+    fused path refuses; DECODE runs three kernels, equal to DECODE_SPLIT."""
     wl = S.WORKLOADS["decode"]
     L = dict(S.make_layer(wl, seed=9, device=DEV))
     L["down_zp"] = None
-    (o1, _, i1), (o2, _, i2) = _both(L, wl)
-    assert torch.equal(i1, i2) and torch.equal(o1, o2)
+    with pytest.raises(B.QMoEError):
+        B.qmoe_forward(L, path=B.PATH_DECODE_FUSED)
+    outs = []
+    for path in (B.PATH_DECODE, B.PATH_DECODE_SPLIT):
+        o, _, i = B.qmoe_forward(L, path=path, return_routing=True)
+        outs.append((o, i))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][0], outs[1][0])
+    assert B.qmoe_forward_kernels(L, 1) == 3
 
 
 def test_kernel_count_query():
     L = S.make_layer(S.WORKLOADS["decode"], seed=10, device=DEV)
     assert B.qmoe_forward_kernels(L, 1) == 1
-    assert B.qmoe_forward_kernels(L, 2) == 1
-    assert B.qmoe_forward_kernels(L, 4) in (1, 3)
+    assert B.qmoe_forward_kernels(L, 2) == 3
+    for T in (1, 2, 3, 4):
+        assert B.qmoe_forward_kernels(L, T, path=B.PATH_DECODE_FUSED) == 1
     assert B.qmoe_forward_kernels(L, 1, path=B.PATH_DECODE_SPLIT) == 3
     assert B.qmoe_forward_kernels(L, 16) == 3
     assert B.qmoe_forward_kernels(L, 512) == 5
