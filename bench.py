@@ -35,7 +35,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel version in this tree has not been captured)
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel from an ncu capture of the current build (None: not yet captured)
-NCU_TRAFFIC = {("prefill", "gateup"): 133138432.0}
+NCU_TRAFFIC = {("prefill", "gateup"): 133138432.0, ("verify", "gateup"): 133650688.0}
 POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24,
         "e128_decode": 24, "e128_prefill": 8, "e256_decode": 24, "e256_prefill": 8}
 DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 60,
