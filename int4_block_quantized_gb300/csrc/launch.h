@@ -52,6 +52,10 @@ cudaError_t launch_unpack_zp(const uint8_t* in, uint8_t* out, int rows, int nb, 
 // does not fit; check_only: plan only, nothing launched
 cudaError_t launch_fused(const FusedParams& f, int act_dtype, int scale_dtype, bool has_zp, cudaStream_t st,
                          bool pdl, bool check_only);
+cudaError_t launch_fused_f16(const FusedParams& f, int scale_dtype, bool has_zp, cudaStream_t st, bool pdl,
+                             bool check_only);
+cudaError_t launch_fused_bf16(const FusedParams& f, int scale_dtype, bool has_zp, cudaStream_t st, bool pdl,
+                              bool check_only);
 
 // prefill path: token gather + tile table, the two grouped GEMMs (mode 0
 // gate-up with SwiGLU, mode 1 down with the weighted scatter-add), and the
