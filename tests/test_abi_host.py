@@ -162,3 +162,42 @@ def test_shared_expert_requires_gate_vector(L):
     from int4_block_quantized_gb300.binding import QWeight
     q = QWeight(FAKE, FAKE, None)
     assert L.qmoe_shared_expert(FAKE, 0, None, q, q, q, 0, 1, 2048, 5632, 32, FAKE, 0, FAKE, 1 << 30, None) == 1
+
+
+def test_adapters_reject_bad_arguments(L):
+    """GPTQ repack / zero-offset / packed zero-point unpack: argument checks
+    happen on the host before anything is enqueued (no GPU needed)."""
+    vp = ctypes.c_void_p
+
+    def repack(**kw):
+        return L.qmoe_repack_gptq(kw.get("qw", FAKE), kw.get("qz", FAKE), kw.get("s", FAKE), kw.get("E", 2),
+                                  kw.get("K", 256), kw.get("N", 64), kw.get("bs", 32), kw.get("off", 1),
+                                  kw.get("offdev", None), kw.get("w", FAKE), kw.get("so", FAKE),
+                                  kw.get("zp", FAKE), None)
+    assert repack(qw=None) == 1
+    assert repack(w=None) == 1
+    assert repack(qz=None) == 1              # zp_out given without qzeros
+    assert repack(zp=None) == 1              # qzeros given without zp_out
+    assert repack(N=60) == 1                 # N not a multiple of 8
+    assert repack(K=48) == 1                 # K not a multiple of 32
+    assert repack(bs=16) == 1                # block size outside {32, 64, 128}
+    assert repack(K=320, bs=128) == 1        # K not a multiple of the block size
+    assert repack(off=2) == 1                # offset 0 or 1 only
+    assert repack(E=0) == 1
+    assert repack(qw=FAKE + 2) == 1          # int32 words must be 4-byte aligned
+    assert repack(s=FAKE + 1) == 1           # scales must be 2-byte aligned
+    assert repack(offdev=vp(FAKE + 2)) == 1  # device offset word must be 4-byte aligned
+    assert L.qmoe_gptq_zero_offset(None, 16, FAKE, None) == 1
+    assert L.qmoe_gptq_zero_offset(FAKE, 0, FAKE, None) == 1
+    assert L.qmoe_gptq_zero_offset(FAKE, 16, None, None) == 1
+    assert L.qmoe_unpack_zero_points(None, 4, 5, FAKE, None) == 1
+    assert L.qmoe_unpack_zero_points(FAKE, 0, 5, FAKE, None) == 1
+    assert L.qmoe_unpack_zero_points(FAKE, 4, 0, FAKE, None) == 1
+
+
+def test_kernel_count_query_rejects_bad_arguments(L):
+    assert L.qmoe_forward_kernels(0, 2048, 1408, 60, 4, 32, 0, 0, 1, 1, 0) == -1
+    assert L.qmoe_forward_kernels(1, 2048, 1408, 60, 61, 32, 0, 0, 1, 1, 0) == -1   # k > E
+    assert L.qmoe_forward_kernels(1, 2048, 1408, 300, 4, 32, 0, 0, 1, 1, 0) == -1   # E > 256
+    assert L.qmoe_forward_kernels(1, 2048, 1408, 60, 4, 48, 0, 0, 1, 1, 0) == -1    # block size
+    assert L.qmoe_forward_kernels(1, 2048, 1408, 60, 4, 32, 0, 0, 1, 1, 6) == -1    # path
