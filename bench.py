@@ -531,9 +531,46 @@ def run_gptq_repack(a):
                       "gpu_launches": 9 * steps}))
 
 
+def run_gptq_repack_reference(a):
+    """--impl reference --config gptq_repack: the plain CPU definition
+    (oracle/formats.py) converting a bounded sample of one layer's GPTQ
+    tensors (row slices of the gate projection), in the same unit."""
+    import numpy as np
+    from oracle import formats as F
+    K, N, bs = 2048, 1408, 32
+    rng = np.random.default_rng(0)
+    ncols = 16  # a sample: 16 output columns of one expert's gate projection
+    qw = rng.integers(0, 2 ** 32, size=(K // 8, ncols), dtype=np.uint64).astype(np.uint32)
+    qz = (rng.integers(0, 2 ** 32, size=(K // bs, ncols // 8), dtype=np.uint64).astype(np.uint32)
+          & np.uint32(0x77777777))
+    sc = rng.integers(0, 2 ** 16, size=(K // bs, ncols), dtype=np.uint64).astype(np.uint16)
+    nbytes = 2 * (qw.nbytes + sc.nbytes) + qz.nbytes + ncols * (K // bs)
+    for _ in range(min(a.warmup, 1)):
+        F.gptq_to_canonical(qw, qz, sc, K, ncols, bs, 1)
+    t0 = time.perf_counter()
+    steps = 0
+    while steps < a.steps and (steps == 0 or time.perf_counter() - t0 < 60.0):
+        F.gptq_to_canonical(qw, qz, sc, K, ncols, bs, 1)
+        steps += 1
+    el = time.perf_counter() - t0
+    gbs = steps * nbytes / el / 1e9
+    sample = "%d conversion(s) of %d output columns of one GPTQ projection (K=%d, bs=%d), python, one thread" % (
+        steps, ncols, K, bs)
+    print(json.dumps({"impl": "reference", "metric": "GPTQ -> canonical weight repack, GB/s (read + write)",
+                      "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup,
+                      "ms_per_step": el / steps * 1e3, "higher_is_better": True, "dtype": "u32/u16/u8",
+                      "data": "synthetic", "config": {"workload": "GPTQ repack, bounded CPU sample"},
+                      "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+                      "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
 def main():
     a = parse()
     if a.config == "gptq_repack":
+        if a.impl == "reference":
+            if int(os.environ.get("RANK", "0")) == 0:
+                run_gptq_repack_reference(a)
+            return
         run_gptq_repack(a)
         return
     from int4_block_quantized_gb300 import synthetic as S
