@@ -82,6 +82,11 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
  *                 without zero points) the whole layer runs as one
  *                 cooperative kernel; otherwise as three kernels (router;
  *                 gate-up + SwiGLU; down + weighted sum).
+ *                 The one-kernel layer is a cooperative launch of one CTA
+ *                 per SM in clusters of 4: it needs the whole GPU, so a
+ *                 context that cannot get every SM (another process under
+ *                 MPS with an SM limit, for one) sees the launch refused
+ *                 (QMOE_ERR_CUDA); DECODE_SPLIT has no such requirement.
  *   DECODE_SPLIT  DECODE as three kernels always.
  *   DECODE_FUSED  DECODE as the one cooperative kernel for T <= 4 (at
  *                 T = 2..4 three kernels are faster on GB300, so DECODE
