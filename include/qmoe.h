@@ -68,6 +68,14 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
 
 /* Path selection for qmoe_forward_ex.
  *   DECODE        per-token GEMV on CUDA cores, fp32 throughout (small T).
+ *                 At T = 1 (gate/up and down either all with or all without
+ *                 zero points, and a shared-memory plan that fits) the whole
+ *                 layer runs as one kernel; otherwise as three kernels
+ *                 (router; gate-up + SwiGLU; down + weighted sum).  The one
+ *                 kernel splits the down projection along I over clusters of
+ *                 4 CTAs and sums the partial outputs in a fixed order; it
+ *                 has no grid-wide wait, so it runs with any number of SMs
+ *                 available, and its results are bit-reproducible.
  *   PREFILL       tokens grouped by expert, grouped GEMM on the tensor cores
  *                 with fp32 accumulation.  Each dequantised weight enters as
  *                 the exact sum of two operands of the activation dtype
@@ -78,22 +86,14 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
  *                 output rounded once to the activation dtype (bf16/fp16),
  *                 about half the tensor-core work; relative error of order
  *                 2^-9 (bf16) of the magnitude of the summed terms.
- *                 At T = 1 (gate/up and down either all with or all
- *                 without zero points) the whole layer runs as one
- *                 cooperative kernel; otherwise as three kernels (router;
- *                 gate-up + SwiGLU; down + weighted sum).
- *                 The one-kernel layer is a cooperative launch of one CTA
- *                 per SM in clusters of 4: it needs the whole GPU, so a
- *                 context that cannot get every SM (another process under
- *                 MPS with an SM limit, for one) sees the launch refused
- *                 (QMOE_ERR_CUDA); DECODE_SPLIT has no such requirement.
  *   DECODE_SPLIT  DECODE as three kernels always.
- *   DECODE_FUSED  DECODE as the one cooperative kernel for T <= 4 (at
- *                 T = 2..4 three kernels are faster on GB300, so DECODE
- *                 does not choose it there); QMOE_ERR_UNSUPPORTED if its
- *                 shared-memory plan does not fit.  The three decode
- *                 variants compute the same arithmetic in the same order:
- *                 results equal bit for bit.
+ *   DECODE_FUSED  DECODE as the one kernel (for T <= 4 where a CTA's share
+ *                 of the selected experts fits in shared memory: at the
+ *                 Qwen1.5-MoE-A2.7B layer shape only T = 1);
+ *                 QMOE_ERR_UNSUPPORTED where it does not fit.  Its routing
+ *                 equals DECODE_SPLIT's bit for bit; its output differs from
+ *                 DECODE_SPLIT's only by the order of fp32 sums in the down
+ *                 projection.
  *   AUTO          DECODE for T <= QMOE_DECODE_MAX_TOKENS, else PREFILL. */
 typedef enum {
   QMOE_PATH_AUTO = 0,
@@ -130,7 +130,12 @@ const char* qmoe_last_cuda_error(void);
  * qmoe_workspace_init; every call leaves it ready for the next one. */
 size_t qmoe_workspace_size(int T, int H, int I, int E, int k);
 
-/* Zero the workspace's control words (counters, device status) on `stream`. */
+/* Zero the workspace's control block (device status, counters, and the
+ * one-kernel decode layer's 128 KB output accumulator) on `stream`.  Every
+ * call leaves the control block ready for the next one; after a call whose
+ * device status reports QMOE_ERR_TIMEOUT or QMOE_ERR_DEVICE_CHECK, run this
+ * again before the workspace's next use (a call that gave up part-way can
+ * leave counters or the accumulator mid-update). */
 int qmoe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Router: logits = x[T,H] . router_w[H,E] (+ router_bias[E]) accumulated in
@@ -199,7 +204,7 @@ int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const fl
 
 /* Number of kernels one qmoe_forward_ex call with these sizes and this path
  * launches on the current device: 1 (decode layer fused into one
- * cooperative kernel), 3 (decode: router, gate-up, down) or 5 (prefill:
+ * kernel), 3 (decode: router, gate-up, down) or 5 (prefill:
  * router, token permutation, two grouped GEMMs, output conversion).  Host
  * only, nothing launched.  Negative status (-QMOE_ERR_*) if the arguments
  * are invalid or the shape is unsupported.  Pointer alignment is not known
@@ -246,9 +251,10 @@ int qmoe_shared_expert(const void* x, int act_dtype, const void* shared_gate_w, 
  *
  * The workspace is a library-owned static device array of
  * QMOE_NOALLOC_SCRATCH_BYTES (2 MiB) per device; the call allocates
- * nothing.  Its first 1 KB (the control block: device status word and the
- * router's grouping counter) starts at zero when the library is loaded and
- * every call leaves the counter at zero again.  The first call on a device
+ * nothing.  Its control block (device status word, counters, the one-kernel
+ * decode layer's output accumulator) starts at zero when the library is
+ * loaded and every call leaves the counters and the accumulator at zero
+ * again.  The first call on a device
  * looks the array's address up (cudaGetSymbolAddress), so make that first
  * call, with the device current, before any stream capture.
  *
@@ -258,12 +264,24 @@ int qmoe_shared_expert(const void* x, int act_dtype, const void* shared_gate_w, 
  * QMOE_ERR_UNSUPPORTED and enqueue nothing; the Qwen1.5-MoE-A2.7B layer
  * shape fits up to T = 16.  Overlapping calls on one device (two streams,
  * or two host threads without ordering) share the array and race: order
- * them on one stream.  The device status word is not reported here. */
+ * them on one stream.  Device-side conditions (a bounded wait that ran out)
+ * are recorded in the scratch's status word: read it with
+ * qmoe_noalloc_status. */
 #define QMOE_NOALLOC_SCRATCH_BYTES (2u << 20)
 int qmoe_forward_noalloc(const void* x, int act_dtype, const void* router_w, const float* router_bias,
                          qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
                          int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,
                          int32_t* topk_ids_out, int accumulate, void* stream);
+
+/* The device status word of qmoe_forward_noalloc's static scratch on the
+ * current device, read and cleared like qmoe_get_device_status (blocking:
+ * synchronises `stream`).  Returns QMOE_OK, or the first QMOE_ERR_* a kernel
+ * recorded since the last read (a bounded wait that ran out, a failed index
+ * or launch-shape check: the output of that call is not valid); *bits_out
+ * (may be NULL) gets the raw bits.  After QMOE_ERR_TIMEOUT the scratch's
+ * counters may be left mid-count: the library has no allocation-free way to
+ * reset them, so such a process should stop using this entry point. */
+int qmoe_noalloc_status(uint32_t* bits_out, void* stream);
 
 /* DequantizeLinear of one [N, K] matrix (packed [N, K/2]) to fp32 out[N,K]:
  * (q - zp) * scale, which fp32 holds exactly. */

@@ -71,6 +71,8 @@ def lib():
         L.qmoe_forward_noalloc.restype = i32
         L.qmoe_forward_noalloc.argtypes = [vp, i32, vp, vp, QWeight, QWeight, QWeight] + [i32] * 7 + \
             [vp, vp, vp, i32, vp]
+        L.qmoe_noalloc_status.restype = i32
+        L.qmoe_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.qmoe_shared_expert.restype = i32
         L.qmoe_shared_expert.argtypes = [vp, i32, vp, QWeight, QWeight, QWeight] + [i32] * 5 + \
             [vp, i32, vp, sz, vp]
@@ -233,6 +235,14 @@ def qmoe_forward_noalloc(layer, x=None, out=None, accumulate=False, return_routi
                                     _stream())
     _check(rc, "qmoe_forward_noalloc")
     return (o, tw, ti) if return_routing else o
+
+
+def qmoe_noalloc_status():
+    """(status code, raw bits) of the static scratch's device status word on
+    the current device; reads and clears it (synchronises the stream)."""
+    bits = ctypes.c_uint32(0)
+    rc = lib().qmoe_noalloc_status(ctypes.byref(bits), _stream())
+    return rc, bits.value
 
 
 def qmoe_forward_kernels(layer, T, path=PATH_AUTO):

@@ -339,6 +339,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
     f.ws_perm = ws.at<int32_t>(L.perm);
     f.user_w = topk_w_out;
     f.user_ids = topk_ids_out;
+    f.acc = ws.at<long long>(L.ctl + kCtlAccOffset);
     if ((rc = mark())) return rc;
     if ((rc = cuda_status(launch_fused(f, act_dtype, scale_dtype, zgu, st, pdl, false)))) return rc;
     return mark();
@@ -520,7 +521,7 @@ int qmoe_get_device_status(void* workspace, uint32_t* bits_out, void* stream) {
     return QMOE_ERR_CUDA;
   if (bits_out) *bits_out = bits;
   if (bits & QMOE_ST_TIMEOUT) return QMOE_ERR_TIMEOUT;
-  if (bits & QMOE_ST_INDEX) return QMOE_ERR_DEVICE_CHECK;
+  if (bits & (QMOE_ST_INDEX | QMOE_ST_RANGE)) return QMOE_ERR_DEVICE_CHECK;
   return QMOE_OK;
 }
 
@@ -538,9 +539,9 @@ namespace {
 
 // 2 MiB: the whole layout of qmoe_workspace_size for the Qwen1.5-MoE-A2.7B
 // layer shape (H = 2048, I = 1408, E = 60, k = 4) at T <= 16 is ~1.3 MB.
-// Zero-initialised at module load, which is what the control block (the
-// first 1 KB: sticky status word and the router's grouping counter) must
-// start as; every call leaves the counter back at zero.
+// Zero-initialised at module load, which is what the control block (status
+// word, counters, the fused decode layer's accumulator) must start as; every
+// call leaves the counters and the accumulator back at zero.
 constexpr size_t kNoAllocScratchBytes = QMOE_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -583,6 +584,14 @@ int qmoe_forward_noalloc(const void* x, int act_dtype, const void* router_w, con
   return forward_impl(x, act_dtype, router_w, router_bias, gate, up, down, scale_dtype, T, H, I, E, k,
                       block_size, out, topk_w_out, topk_ids_out, accumulate, QMOE_PATH_AUTO, scratch,
                       kNoAllocScratchBytes, stream, nullptr, 0);
+}
+
+int qmoe_noalloc_status(uint32_t* bits_out, void* stream) {
+  int rc = QMOE_OK;
+  void* scratch = noalloc_scratch_ptr(&rc);
+  if (!scratch) return rc;
+  // the status word is the first word of the scratch's control block
+  return qmoe_get_device_status(scratch, bits_out, stream);
 }
 
 }  // extern "C"

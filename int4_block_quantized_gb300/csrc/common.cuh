@@ -285,8 +285,14 @@ __device__ __forceinline__ void softmax_topk(const float (&lg)[ME], int E, int k
   float mx = -INFINITY;
 #pragma unroll
   for (int m = 0; m < ME; ++m) mx = fmaxf(mx, lg[m]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  {
+    // warp max through the integer reduction unit: floats mapped to
+    // unsigned keys with the same order
+    uint32_t key = __float_as_uint(mx);
+    key = (key & 0x80000000u) ? ~key : (key | 0x80000000u);
+    key = __reduce_max_sync(0xffffffffu, key);
+    mx = __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+  }
   float pr[ME];
   if (gate_sigmoid) {
 #pragma unroll
@@ -309,25 +315,23 @@ __device__ __forceinline__ void softmax_topk(const float (&lg)[ME], int E, int k
     wts[j] = 0.f;
   }
   for (int j = 0; j < k; ++j) {
-    float bp = -1.f;
+    // the largest remaining probability (p >= 0: its bits order as
+    // unsigned integers; + 1 keeps p = 0 above "no candidate"), then the
+    // lowest expert id holding it, each by one warp reduction
+    uint32_t bkey = 0u;
     int bi = 0x7fffffff;
 #pragma unroll
     for (int m = 0; m < ME; ++m) {
       const int e = lane + 32 * m;
-      if (e < E && !((chosen >> m) & 1u) && pr[m] > bp) {
-        bp = pr[m];
+      const uint32_t key = __float_as_uint(pr[m]) + 1u;
+      if (e < E && !((chosen >> m) & 1u) && key > bkey) {
+        bkey = key;
         bi = e;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (op > bp || (op == bp && oi < bi)) {
-        bp = op;
-        bi = oi;
-      }
-    }
+    const uint32_t mkey = __reduce_max_sync(0xffffffffu, bkey);
+    bi = (int)__reduce_min_sync(0xffffffffu, bkey == mkey ? (uint32_t)bi : 0xffffffffu);
+    const float bp = __uint_as_float(mkey - 1u);
     if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
     // (select, not index: a runtime index would put the arrays in local memory)
 #pragma unroll

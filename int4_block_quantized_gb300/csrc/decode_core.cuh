@@ -79,18 +79,6 @@ struct DecodePlan {
   uint32_t res_off, stage_off, slot_base, smem;
 };
 
-// Shared-memory plan of the fused layer: the two phases' rings (gate-up,
-// down) side by side, the router's scratch laid over them.
-struct FusedPlan {
-  DecodePlan g, d;           // slot_rows, max_stages, nslots per phase
-  uint32_t res_off;          // x in decode layout (gate-up), then the down partials
-  uint32_t stg_off, std_off;  // stage tables
-  uint32_t ring_g, ring_d, smem;
-  uint32_t slot_g, slot_d;   // slot strides
-  int pass_rows;             // router rows staged per pass
-  uint32_t xs_off, part_off, vpart_off, wch_off;
-};
-
 // ---------------------------------------------------------------- dequant
 // A register the compiler cannot fold back into an immediate, so that
 // (v & MASK) | magic is a single three-input LOP3.

@@ -17,6 +17,7 @@ namespace qmoe {
 // ---- device status word bits (workspace control block, word 0)
 constexpr uint32_t QMOE_ST_TIMEOUT = 1u;  // a bounded wait ran out
 constexpr uint32_t QMOE_ST_INDEX = 2u;    // an index check failed
+constexpr uint32_t QMOE_ST_RANGE = 4u;    // a value beyond a fixed-point accumulator's range
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 8;
@@ -25,9 +26,14 @@ constexpr int kMaxTopk = 8;
 constexpr int kCtlStatus = 0;         // u32 sticky status bits
 constexpr int kCtlGroupTicket = 1;    // u32 router: token tiles done with top-k
 constexpr int kCtlNtiles = 2;         // u32 prefill: number of token tiles
-constexpr int kCtlGridCount = 3;      // u32 fused decode: grid-barrier arrivals (reset by the last)
-constexpr int kCtlGridGen = 4;        // u32 fused decode: grid-barrier generation
-constexpr size_t kCtlBytes = 1024;
+constexpr int kCtlSliceDone = 8;      // u32 x kMaxSplit, fused decode: clusters done with each output
+                                      // slice (reset to 0 by the last arrival)
+// fused decode: int64 fixed-point (2^-32) output accumulator [T][H], zero
+// between calls (each call's last arrivals read and clear what it used)
+constexpr size_t kCtlAccOffset = 1024;
+constexpr size_t kCtlAccBytes = 128 * 1024;
+constexpr int kCtlAccElems = (int)(kCtlAccBytes / 8);
+constexpr size_t kCtlBytes = kCtlAccOffset + kCtlAccBytes;
 
 // ---- router tiling
 constexpr int kRouteThreads = 256;
@@ -178,8 +184,8 @@ struct DecodeParams {
   uint32_t* ctl;
 };
 
-// Fused decode layer (router + gate-up + down in one cooperative launch,
-// T <= kTokGroup): the gate-up and down views of the weights plus the router.
+// Fused decode layer (router + gate-up + down in one launch, T <= kTokGroup):
+// the gate-up and down views of the weights plus the router.
 struct FusedParams {
   DecodeParams g, d;
   const void* x;          // [T, H] 16-bit
@@ -194,6 +200,7 @@ struct FusedParams {
   int32_t* ws_perm;
   float* user_w;          // optional user copies of the top-k
   int32_t* user_ids;
+  long long* acc;         // [T][H] int64 fixed-point output accumulator (control block)
 };
 
 // Prefill path (grouped GEMM on the tensor cores).  The token tile table

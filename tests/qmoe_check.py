@@ -67,3 +67,31 @@ def check_routing(gpu_ids, gpu_w, probs, ref_ids, k):
     pw = np.take_along_axis(probs, gpu_ids.astype(np.int64), axis=1)
     np.testing.assert_allclose(gw, pw, rtol=1e-5, atol=1e-7)
     return near
+
+
+def run_layer_and_check(wl, L, path, accumulate=False, seed=0):
+    """Run one qmoe_forward through the C ABI on `path` and compare it with
+    the fp64 oracle (routing with the near-tie rule, output elementwise).
+    Returns (output, topk weights, topk ids, worst relative error, near-tie count)."""
+    import oracle
+    from int4_block_quantized_gb300 import binding as B
+    x = L["x"]
+    out0 = None
+    out = None
+    if accumulate:
+        out0 = torch.randn(x.shape, generator=torch.Generator(device=x.device).manual_seed(seed + 7),
+                           device=x.device).to(x.dtype)
+        out = out0.clone()
+    ws = B.Workspace(x.shape[0], wl.H, wl.I, wl.E, wl.k, device=x.device)
+    o, tw, ti = B.qmoe_forward(L, out=out, ws=ws, accumulate=accumulate, path=path, return_routing=True)
+    torch.cuda.synchronize()
+    assert ws.status() == (0, 0)
+    ref, ref_ids, ref_w, probs = oracle.qmoe_forward(L)
+    ids = ti.cpu().numpy()
+    near = check_routing(ids, tw.cpu().numpy(), probs, ref_ids, wl.k)
+    if near.any():
+        ref2, _, _, _ = oracle.qmoe_forward(L, forced_ids=ids, forced_w=tw.cpu().double().numpy())
+        ref[near] = ref2[near]
+    if accumulate:
+        ref = ref + out0.double().cpu().numpy()
+    return o, tw, ti, assert_close_layer(o, ref, wl.name), int(near.sum())

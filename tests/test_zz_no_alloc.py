@@ -27,6 +27,7 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
     for _ in range(2):  # the second call sees the scratch the first one left
         o, tw, ti = B.qmoe_forward_noalloc(L, return_routing=True)
         torch.cuda.synchronize()
+        assert B.qmoe_noalloc_status() == (0, 0)
         assert torch.equal(ti, ri)
         assert torch.allclose(tw, rw, rtol=0, atol=1e-6)
         assert_close_layer(o, to_f64(ref), name + " noalloc")
@@ -38,6 +39,7 @@ def test_noalloc_residual_accumulate():
     base = torch.randn(wl.T, wl.H, generator=torch.Generator(device=DEV).manual_seed(5), device=DEV).half()
     ref = B.qmoe_forward(L, out=base.clone(), accumulate=True)
     o = B.qmoe_forward_noalloc(L, out=base.clone(), accumulate=True)
+    assert B.qmoe_noalloc_status() == (0, 0)
     assert_close_layer(o, to_f64(ref), "noalloc accumulate")
 
 
