@@ -77,15 +77,24 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
  *                 has no grid-wide wait, so it runs with any number of SMs
  *                 available, and its results are bit-reproducible.
  *   PREFILL       tokens grouped by expert, grouped GEMM on the tensor cores
- *                 with fp32 accumulation.  Each dequantised weight enters as
- *                 the exact sum of two operands of the activation dtype
- *                 (hi = RN(w), lo = w - hi), and the SwiGLU output likewise,
- *                 so the only roundings are fp32 accumulation, the 16+16-bit
- *                 SwiGLU output and the final output.
- *   PREFILL_FAST  the same GEMM with single operands: weights and SwiGLU
- *                 output rounded once to the activation dtype (bf16/fp16),
- *                 about half the tensor-core work; relative error of order
- *                 2^-9 (bf16) of the magnitude of the summed terms.
+ *                 with fp32 accumulation and exact operands: with bf16 block
+ *                 scales the operands are fp16 (bf16 activations convert
+ *                 exactly within fp16's normal range) and, without zero
+ *                 points, each dequantised weight is one fp16 operand
+ *                 (s (q - 8) has at most 11 significant bits); with zero
+ *                 points or fp16 scales each weight is the exact sum of two
+ *                 operands (hi = RN(w), lo = w - hi) of fp16, or of bf16
+ *                 for bf16 activations with fp16 scales.  The SwiGLU
+ *                 output enters the down projection as hi + lo of the
+ *                 operand type.  So the only roundings are fp32
+ *                 accumulation, the hi + lo SwiGLU output and the final
+ *                 output (on the fp16 operands, values below fp16's
+ *                 normal range, 2^-14, round to its subnormals: an absolute
+ *                 error of at most 2^-25).  A bf16 activation or SwiGLU value beyond fp16's
+ *                 range (65504) on the fp16-operand form sets a device
+ *                 status bit (QMOE_ERR_DEVICE_CHECK).  (Value 3 of this
+ *                 enum is not used: a single-rounded-operand form that
+ *                 missed the elementwise tolerance was withdrawn.)
  *   DECODE_SPLIT  DECODE as three kernels always.
  *   DECODE_FUSED  DECODE as the one kernel (for T <= 4 where a CTA's share
  *                 of the selected experts fits in shared memory: at the
@@ -99,7 +108,6 @@ typedef enum {
   QMOE_PATH_AUTO = 0,
   QMOE_PATH_DECODE = 1,
   QMOE_PATH_PREFILL = 2,
-  QMOE_PATH_PREFILL_FAST = 3,
   QMOE_PATH_DECODE_SPLIT = 4,
   QMOE_PATH_DECODE_FUSED = 5
 } qmoe_path;
@@ -168,12 +176,12 @@ int matmul_nbits(const void* x, int act_dtype, const uint8_t* w, const void* sca
  * IR guide section 2 "Quantization Scheme" for the weight format and the
  * dequantize-then-matmul definition).  path:
  *   DECODE        the CUDA-core path above (workspace unused, may be NULL);
- *   PREFILL       tensor cores (tcgen05) on the exact split of each
- *                 dequantised weight into bf16/fp16 hi + lo parts, as in the
- *                 layer's down projection with one expert of weight 1;
- *   PREFILL_FAST  the same with the weight rounded once to act_dtype;
+ *   PREFILL       tensor cores (tcgen05) with exact operands as in the
+ *                 layer's prefill path (one fp16 weight operand for bf16
+ *                 scales without zero points, else hi + lo) and x as one
+ *                 operand;
  *   AUTO          DECODE for M <= QMOE_DECODE_MAX_TOKENS, else PREFILL.
- * The tensor-core paths need N % 128 == 0, K % 64 == 0, x, y, scales and
+ * The tensor-core path needs N % 128 == 0, K % 64 == 0, x, y, scales and
  * zero points 16-byte aligned and an initialised workspace (qmoe_workspace_init)
  * of at least qmoe_workspace_size(M, N, K, 1, 1) bytes (QMOE_ERR_WORKSPACE if
  * smaller); other shapes return QMOE_ERR_UNSUPPORTED.  y is fully written;

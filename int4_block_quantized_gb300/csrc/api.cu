@@ -183,7 +183,7 @@ int matmul_nbits(const void* x, int act_dtype, const uint8_t* w, const void* sca
 int matmul_nbits_ex(const void* x, int act_dtype, const uint8_t* w, const void* scales, int scale_dtype,
                     const uint8_t* zp, int M, int N, int K, int block_size, void* y, int path, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_PREFILL_FAST) return QMOE_ERR_INVALID_ARG;
+  if (path != QMOE_PATH_AUTO && path != QMOE_PATH_DECODE && path != QMOE_PATH_PREFILL) return QMOE_ERR_INVALID_ARG;
   if (path == QMOE_PATH_DECODE || (path == QMOE_PATH_AUTO && M <= kDecodeMaxTokens))
     return matmul_nbits(x, act_dtype, w, scales, scale_dtype, zp, M, N, K, block_size, y, stream);
   if (!x || !y || !valid_dtype(act_dtype) || !valid_dtype(scale_dtype)) return QMOE_ERR_INVALID_ARG;
@@ -196,8 +196,8 @@ int matmul_nbits_ex(const void* x, int act_dtype, const uint8_t* w, const void* 
   // the GEMM's view: one expert with N rows and a K-long reduction, M tokens
   const WsLayout L = ws_layout(M, N, K, 1, 1);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
-  const bool split = path != QMOE_PATH_PREFILL_FAST;
-  if (!dense_fits(N, K, block_size, zp != nullptr, split) || !aligned(scales, 16) || !aligned(zp, 16))
+  if (!dense_fits(N, K, block_size, act_dtype, scale_dtype, zp != nullptr) || !aligned(scales, 16) ||
+      !aligned(zp, 16))
     return QMOE_ERR_UNSUPPORTED;
   if ((rc = check_device())) return rc;
   Ws ws{L, static_cast<uint8_t*>(workspace)};
@@ -211,13 +211,14 @@ int matmul_nbits_ex(const void* x, int act_dtype, const uint8_t* w, const void* 
   p.perm = ws.at<int32_t>(L.perm);
   p.topk_w = ws.at<float>(L.w);
   p.act = ws.at<uint16_t>(L.act16);
-  p.act_lo = split ? ws.at<uint16_t>(L.act16lo) : nullptr;
+  p.act_lo = nullptr;  // x is exact in one operand
+  p.x_to_f16 = prefill_x_to_f16(act_dtype, scale_dtype);
   p.out_acc = ws.at<float>(L.outacc);
   p.tiles = ws.at<int32_t>(L.tiles);
   p.ctl = ws.at<uint32_t>(L.ctl);
   cudaStream_t st = (cudaStream_t)stream;
   if ((rc = cuda_status(launch_dense_setup(p, x, st, true)))) return rc;
-  if ((rc = cuda_status(launch_prefill_gemm(p, 1, act_dtype, scale_dtype, split, st, true)))) return rc;
+  if ((rc = cuda_status(launch_prefill_gemm(p, 1, act_dtype, scale_dtype, true, st, true)))) return rc;
   return cuda_status(launch_prefill_convert(p, y, act_dtype, st, true));
 }
 
@@ -253,7 +254,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
       (rc = check_qweight(down, H, I, block_size)))
     return rc;
   if ((gate.zp == nullptr) != (up.zp == nullptr)) return QMOE_ERR_INVALID_ARG;
-  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_FUSED) return QMOE_ERR_INVALID_ARG;
+  if (path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_FUSED || path == 3) return QMOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(T, H, I, E, k);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return QMOE_ERR_WORKSPACE;
   if ((rc = check_device())) return rc;
@@ -261,8 +262,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   const bool dec_ok = T <= kDecodeMaxTokens && decode_fits(kModeGateUp, T, I, H, block_size, zgu, k) &&
                       decode_fits(kModeDown, T, H, I, block_size, zd, k);
   // the grouped GEMM copies whole rows of scales / zero points in bulk: 16-byte aligned bases
-  const bool split = path != QMOE_PATH_PREFILL_FAST;
-  const bool pre_ok = prefill_fits(H, I, block_size, zgu, zd, split) && aligned(gate.scales, 16) &&
+  const bool pre_ok = prefill_fits(H, I, block_size, act_dtype, scale_dtype, zgu, zd) && aligned(gate.scales, 16) &&
                       aligned(up.scales, 16) && aligned(down.scales, 16) && aligned(gate.zp, 16) &&
                       aligned(up.zp, 16) && aligned(down.zp, 16);
   const bool split_decode = path == QMOE_PATH_DECODE_SPLIT;
@@ -270,7 +270,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   if (split_decode || force_fused) path = QMOE_PATH_DECODE;
   if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
   if (path == QMOE_PATH_DECODE && !dec_ok) return QMOE_ERR_UNSUPPORTED;
-  if ((path == QMOE_PATH_PREFILL || path == QMOE_PATH_PREFILL_FAST) && !pre_ok) return QMOE_ERR_UNSUPPORTED;
+  if (path == QMOE_PATH_PREFILL && !pre_ok) return QMOE_ERR_UNSUPPORTED;
 
   Ws ws{L, static_cast<uint8_t*>(workspace)};
   cudaStream_t st = (cudaStream_t)stream;
@@ -350,7 +350,7 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
                      nullptr, nullptr, st, pdl, gate_sigmoid);
   if (rc || (rc = mark())) return rc;
 
-  if (path == QMOE_PATH_PREFILL || path == QMOE_PATH_PREFILL_FAST) {
+  if (path == QMOE_PATH_PREFILL) {
     PrefillParams p = {};
     const qmoe_qweight* q[3] = {&gate, &up, &down};
     for (int m = 0; m < 3; ++m) {
@@ -366,15 +366,16 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
     p.xp = ws.at<uint16_t>(L.xp);
     p.act = ws.at<uint16_t>(L.act16);
     p.act_lo = ws.at<uint16_t>(L.act16lo);
+    p.x_to_f16 = prefill_x_to_f16(act_dtype, scale_dtype);
     p.out_acc = ws.at<float>(L.outacc);
     p.tiles = ws.at<int32_t>(L.tiles);
     p.ctl = ws.at<uint32_t>(L.ctl);
     p.accumulate = accumulate;
     rc = cuda_status(launch_prefill_permute(p, x, act_dtype, st, pdl));
     if (rc || (rc = mark())) return rc;
-    rc = cuda_status(launch_prefill_gemm(p, 0, act_dtype, scale_dtype, split, st, pdl));
+    rc = cuda_status(launch_prefill_gemm(p, 0, act_dtype, scale_dtype, false, st, pdl));
     if (rc || (rc = mark())) return rc;
-    rc = cuda_status(launch_prefill_gemm(p, 1, act_dtype, scale_dtype, split, st, pdl));
+    rc = cuda_status(launch_prefill_gemm(p, 1, act_dtype, scale_dtype, false, st, pdl));
     if (rc || (rc = mark())) return rc;
     rc = cuda_status(launch_prefill_convert(p, out, act_dtype, st, pdl));
     if (rc) return rc;
@@ -405,14 +406,15 @@ int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const fl
 int qmoe_forward_kernels(int T, int H, int I, int E, int k, int block_size, int act_dtype, int scale_dtype,
                          int gate_up_has_zp, int down_has_zp, int path) {
   if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1 || k > E || E > kMaxExperts || k > kMaxTopk || !valid_dtype(act_dtype) ||
-      !valid_dtype(scale_dtype) || !valid_bs(block_size) || path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_FUSED)
+      !valid_dtype(scale_dtype) || !valid_bs(block_size) || path < QMOE_PATH_AUTO || path > QMOE_PATH_DECODE_FUSED ||
+      path == 3)
     return -QMOE_ERR_INVALID_ARG;
   int rc = check_device();
   if (rc) return -rc;
   const bool zgu = gate_up_has_zp != 0, zd = down_has_zp != 0;
   const bool dec_ok = T <= kDecodeMaxTokens && decode_fits(kModeGateUp, T, I, H, block_size, zgu, k) &&
                       decode_fits(kModeDown, T, H, I, block_size, zd, k);
-  const bool pre_ok = prefill_fits(H, I, block_size, zgu, zd, path != QMOE_PATH_PREFILL_FAST);
+  const bool pre_ok = prefill_fits(H, I, block_size, act_dtype, scale_dtype, zgu, zd);
   if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
   if (path == QMOE_PATH_DECODE || path == QMOE_PATH_DECODE_SPLIT || path == QMOE_PATH_DECODE_FUSED) {
     if (!dec_ok) return -QMOE_ERR_UNSUPPORTED;

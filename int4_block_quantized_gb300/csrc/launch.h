@@ -60,13 +60,15 @@ cudaError_t launch_fused_bf16(const FusedParams& f, int scale_dtype, bool has_zp
 // prefill path: token gather + tile table, the two grouped GEMMs (mode 0
 // gate-up with SwiGLU, mode 1 down with the weighted scatter-add), and the
 // final fp32 -> act_dtype conversion (plus residual)
-bool prefill_fits(int H, int I, int bs, bool has_zp_gu, bool has_zp_d, bool split);
+bool prefill_fits(int H, int I, int bs, int act_dtype, int scale_dtype, bool has_zp_gu, bool has_zp_d);
 // dense MatMulNBits on the grouped GEMM (down mode, one expert): N outputs, K inputs
-bool dense_fits(int N, int K, int bs, bool has_zp, bool split);
+bool dense_fits(int N, int K, int bs, int act_dtype, int scale_dtype, bool has_zp);
+// true if the GEMM's operands are fp16 while x is bf16 (x converted on gather)
+bool prefill_x_to_f16(int act_dtype, int scale_dtype);
 cudaError_t launch_dense_setup(const PrefillParams& p, const void* x, cudaStream_t st, bool pdl);
 cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int act_dtype, cudaStream_t st,
                                    bool pdl);
-cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype, int scale_dtype, bool split,
+cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype, int scale_dtype, bool dense,
                                 cudaStream_t st, bool pdl);
 cudaError_t launch_prefill_convert(const PrefillParams& p, void* out, int act_dtype, cudaStream_t st,
                                    bool pdl);

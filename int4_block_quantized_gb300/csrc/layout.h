@@ -220,6 +220,7 @@ struct PrefillParams {
   int32_t* tiles;           // [ntiles][4]
   uint32_t* ctl;            // control block (status, tile count)
   int accumulate;
+  int x_to_f16;             // gather / dense setup convert bf16 x to the fp16 operands
   int nst, nsz, npk;        // operand stages, tile scale buffers, packed-code slots (per GEMM launch)
 };
 

@@ -23,10 +23,14 @@
 //   one thread issues tcgen05.mma into a double-buffered TMEM accumulator;
 //   four epilogue warps tcgen05.ld it and apply SwiGLU or the weighted
 //           fp32 scatter-add.
-// A dequantised weight w = (q - zp) * s enters the MMAs as hi = RN(w) plus
-// lo = w - hi (an exact sum), or as hi alone on the fast path; K is permuted
-// inside every group of 8 (order 0,4,1,5,2,6,3,7) identically for weights
-// and activations so one LOP3 yields two operands from a 32-bit word.
+// Operands are exact.  With bf16 block scales a dequantised weight w = (q -
+// zp) * s has at most 12 significant bits and enters as one fp16 operand
+// (the activations converted to fp16 as well, exactly in fp16's range);
+// with fp16 scales it has up to 15 and enters as hi = RN(w) plus lo = w - hi
+// in the activation dtype.  The SwiGLU output enters the down GEMM as
+// hi + lo likewise.  K is permuted inside every group of 8 (order
+// 0,4,1,5,2,6,3,7) identically for weights and activations so one LOP3
+// yields two operands from a 32-bit word.
 #include <cuda.h>
 #include <math.h>
 
@@ -46,6 +50,21 @@ constexpr int kModeGU = 0, kModeDN = 1;
 // position of element j (0..7) of a group of 8 in the permuted K order
 __host__ __device__ __forceinline__ int kperm_pos(int j) { return (j & 3) * 2 + (j >> 2); }
 
+
+// Eight bf16 values to fp16 (exact inside fp16's range; a value beyond it
+// sets QMOE_ST_RANGE).
+__device__ __forceinline__ uint4 bf16x8_to_f16(uint4 v, uint32_t* status) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  bool big = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
+    big |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+    w[i] = (uint32_t)__half_as_ushort(__float2half_rn(a)) | ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+  }
+  if (big) set_status(status, QMOE_ST_RANGE);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // ---------------------------------------------------------------- permute
 // xp[r] = x[token of sorted assignment r] with K permuted inside each group
@@ -90,7 +109,8 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint16_t* __restrict
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(p.xp + (size_t)r * H);
     for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-      const uint4 v = __ldg(src + g);
+      uint4 v = __ldg(src + g);
+      if (p.x_to_f16) v = bf16x8_to_f16(v, p.ctl + kCtlStatus);
       uint4 o;  // (e0,e1,..,e7) -> (e0,e4,e1,e5,e2,e6,e3,e7)
       o.x = __byte_perm(v.x, v.z, 0x5410);
       o.y = __byte_perm(v.x, v.z, 0x7632);
@@ -144,7 +164,8 @@ __global__ void __launch_bounds__(256) dense_setup_kernel(const uint16_t* __rest
   uint4* dst = reinterpret_cast<uint4*>(p.act);
   uint4* dlo = reinterpret_cast<uint4*>(p.act_lo);
   for (size_t i = t0; i < ng; i += stride) {
-    const uint4 v = __ldg(src + i);
+    uint4 v = __ldg(src + i);
+    if (p.x_to_f16) v = bf16x8_to_f16(v, p.ctl + kCtlStatus);
     uint4 o;  // (e0,e1,..,e7) -> (e0,e4,e1,e5,e2,e6,e3,e7)
     o.x = __byte_perm(v.x, v.z, 0x5410);
     o.y = __byte_perm(v.x, v.z, 0x7632);
@@ -299,9 +320,11 @@ struct GemmSmem {
   uint32_t a_lo, b_hi, b_lo, stage;  // offsets inside an operand stage, stage size
   uint32_t sz_bytes, sz_off, stage_off, pk_off, gbuf_off, total;
 };
-__host__ __device__ inline GemmSmem gemm_smem(int mode, bool split, int nb, bool has_zp, int nst, int nsz, int npk) {
+// ws: weights as hi + lo operands; as: activations (down: SwiGLU output) as hi + lo
+__host__ __device__ inline GemmSmem gemm_smem(int mode, bool ws, bool as, int nb, bool has_zp, int nst, int nsz,
+                                              int npk) {
   GemmSmem S;
-  const uint32_t na = split ? 2 : 1, nbt = (split && mode == kModeDN) ? 2 : 1;
+  const uint32_t na = ws ? 2 : 1, nbt = as ? 2 : 1;
   S.a_lo = kTileOp;
   S.b_hi = na * kTileOp;
   S.b_lo = S.b_hi + kTileOp;
@@ -320,12 +343,12 @@ __host__ __device__ inline GemmSmem gemm_smem(int mode, bool split, int nb, bool
 // else 2; the packed ring takes the rest (<= 24 slots).  Long reductions
 // with small blocks (large whole-K scale buffers) fall back to one scale
 // buffer and as few as 4 packed slots.
-__host__ inline bool gemm_plan(int mode, bool split, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
+__host__ inline bool gemm_plan(int mode, bool ws, bool as, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
   for (int sz = 2; sz >= 1; --sz)
     for (int st = 3; st >= 2; --st) {
       const int pmin = sz == 1 && st == 2 ? 4 : 8;
       int pk = kMaxPk;
-      while (pk >= pmin && gemm_smem(mode, split, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
+      while (pk >= pmin && gemm_smem(mode, ws, as, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
       if (pk >= pmin) {
         nst = st;
         nsz = sz;
@@ -376,7 +399,8 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int n, int issued) {
 // One persistent CTA per SM.  Work item t = (weight row block mb, token
 // tile nt), nt fastest, so the token tiles of one expert run side by side
 // and share the weight tile through L2.
-template <int MODE, typename TA, typename TS, bool HAS_ZP, bool SPLIT>
+// OT: operand type (fp16 / bf16); WS / AS as for gemm_smem
+template <int MODE, typename OT, typename TS, bool HAS_ZP, bool WS, bool AS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                 const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
@@ -384,12 +408,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   constexpr bool GU = MODE == kModeGU;
-  constexpr bool BLO = SPLIT && !GU;  // second B tile (activation low part)
+  constexpr bool BLO = AS && !GU;  // second B tile (activation low part)
   const int K = GU ? p.H : p.I;       // reduction length
   const int NR = GU ? p.I : p.H;      // weight rows per expert matrix
   const int nb = K >> p.lbs;
   const int nst = p.nst, nsz = p.nsz, npk = p.npk;
-  const GemmSmem L = gemm_smem(MODE, SPLIT, nb, HAS_ZP, nst, nsz, npk);
+  const GemmSmem L = gemm_smem(MODE, WS, BLO, nb, HAS_ZP, nst, nsz, npk);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint64_t* b_full = bars;                  // [4] token tile landed
   uint64_t* a_full = bars + 4;              // [4] operand dequantised (one arrival per dequant warp)
@@ -528,7 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int tc = 0;
       bool issued = false;
       Ring rs;
-      constexpr bool bf = std::is_same<TA, __nv_bfloat16>::value;
+      constexpr bool bf = std::is_same<OT, __nv_bfloat16>::value;
       for (int t = blockIdx.x; t < ntile_total; t += gridDim.x, ++tc) {
         const int4 tl = __ldcg(tiles + t % NT);
         const uint32_t idesc = idesc_f16(128, (tl.z + 15) & ~15, bf);
@@ -550,7 +574,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // K = 16 per instruction: +32 bytes in the swizzled row
             mma_f16_ss(d_tmem, ah + 2 * kk, bh + 2 * kk, idesc, (kc | kk) != 0);
-            if (SPLIT) mma_f16_ss(d_tmem, al + 2 * kk, bh + 2 * kk, idesc, 1u);
+            if (WS) mma_f16_ss(d_tmem, al + 2 * kk, bh + 2 * kk, idesc, 1u);
             if (BLO) mma_f16_ss(d_tmem, ah + 2 * kk, bl + 2 * kk, idesc, 1u);
           }
           issued = true;
@@ -571,18 +595,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int it = 0;
     Ring rs, rp, rz;
     bool ok = true;
+    // The rows of a tile's scales sit nb * 2 bytes apart: at 128 bytes the 32
+    // rows of a warp fall into one bank.  When rows are 16-byte aligned a
+    // lane reads 8 consecutive block scales (and 8 zero points) at once and
+    // keeps them for the next chunks: one conflicted load per 8 blocks.
+    const bool vec = (nb & 7) == 0;
     for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x, rz.next(nsz)) {
       if (!wait_or_abort(&sz_full[rz.i], rz.ph, status, s_abort)) break;
       const uint8_t* sz = szbuf + rz.i * L.sz_bytes;
       const uint16_t* srow = reinterpret_cast<const uint16_t*>(sz) + (size_t)r * nb;
       const uint8_t* zrow = sz + 128u * nb * 2 + (size_t)r * nb;
+      int cached = -8;
+      uint4 sv = make_uint4(0, 0, 0, 0);
+      uint2 zv = make_uint2(0, 0);
       for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst), rp.next(npk)) {
         if (!wait_or_abort(&pk_full[rp.i], rp.ph, status, s_abort)) { ok = false; break; }
         const uint4 q = *reinterpret_cast<const uint4*>(pkbuf + rp.i * kPkBytes + r * 32 + hh * 16);
         // block_size >= 32: the 32 codes of this half share one block
         const int blk = (kc * 64 + hh * 32) >> p.lbs;
-        Deq<TA, TS> d;
-        d.set(HAS_ZP ? (uint32_t)zrow[blk] : 8u, srow[blk]);
+        uint32_t zpv;
+        uint16_t scv;
+        if (vec) {
+          if ((blk & ~7) != cached) {
+            cached = blk & ~7;
+            sv = *reinterpret_cast<const uint4*>(srow + cached);
+            if (HAS_ZP) zv = *reinterpret_cast<const uint2*>(zrow + cached);
+          }
+          const int j = blk & 7;
+          const uint32_t sw = (j >> 1) == 0 ? sv.x : (j >> 1) == 1 ? sv.y : (j >> 1) == 2 ? sv.z : sv.w;
+          scv = (uint16_t)(sw >> ((j & 1) * 16));
+          zpv = HAS_ZP ? (((j >> 2) ? zv.y : zv.x) >> ((j & 3) * 8)) & 0xFFu : 8u;
+        } else {
+          scv = srow[blk];
+          zpv = HAS_ZP ? (uint32_t)zrow[blk] : 8u;
+        }
+        Deq<OT, TS> d;
+        d.set(zpv, scv);
         if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) { ok = false; break; }
         uint8_t* st = stages + rs.i * L.stage;
         const uint32_t roff = (r >> 3) * 1024 + (r & 7) * 128;
@@ -592,7 +640,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int g = hh * 4 + gg;
           const uint32_t off = roff + ((g ^ (r & 7)) << 4);  // 128-byte swizzle
           uint4 h, l;  // elements (0,4), (1,5), (2,6), (3,7) of the group
-          if (SPLIT) {
+          if (WS) {
             d.both(w[gg], h.x, l.x);
             d.both(w[gg] >> 4, h.y, l.y);
             d.both(w[gg] >> 8, h.z, l.z);
@@ -659,14 +707,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float g = gx[i * 17 + j];
                 const float a = g / (1.f + expf(-g)) * __uint_as_float(v[j]);
                 const size_t o = (size_t)(row0 + c0 + j) * p.I + col;
-                if (SPLIT) {
-                  uint16_t h, l;
-                  split_act<TA>(a, h, l);
-                  p.act[o] = h;
-                  p.act_lo[o] = l;
-                } else {
-                  p.act[o] = Half<TA>::from_float(a);
-                }
+                uint16_t h, l;
+                split_act<OT>(a, h, l);
+                if (std::is_same<OT, __half>::value && !(fabsf(a) <= 65504.f)) set_status(status, QMOE_ST_RANGE);
+                p.act[o] = h;
+                p.act_lo[o] = l;
               }
             }
             __syncwarp();
@@ -706,17 +751,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ---------------------------------------------------------------- host
 
-bool dense_fits(int N, int K, int bs, bool has_zp, bool split) {
-  if (N % 128 || K % 64 || bs < 32 || (bs & (bs - 1))) return false;
-  int a, b, c;
-  return gemm_plan(kModeDN, split, K / bs, has_zp, a, b, c);
+// Operands of the grouped GEMM.  The operand type is fp16 when the block
+// scales are bf16 or the activations fp16 (a bf16 token converts to fp16
+// exactly inside fp16's normal range), else bf16.  One weight operand is
+// exact when the scales are bf16 and there are no zero points: q - 8 lies in
+// [-8, 7], whose magnitudes need at most 3 significant bits (8 needs one),
+// so s (q - 8) has at most 8 + 3 = 11, fp16's significand.  With zero points
+// q - zp reaches 15 (4 bits) and fp16 scales carry 11 bits, so those weights
+// go hi + lo (the product's leading 11 bits, then the rest).
+struct GemmOps {
+  bool f16, ws;
+};
+static inline GemmOps gemm_ops(int act_dtype, int scale_dtype, bool has_zp) {
+  return {scale_dtype == 1 || act_dtype == 0, scale_dtype == 0 || has_zp};
 }
 
-bool prefill_fits(int H, int I, int bs, bool has_zp_gu, bool has_zp_d, bool split) {
+bool dense_fits(int N, int K, int bs, int act_dtype, int scale_dtype, bool has_zp) {
+  if (N % 128 || K % 64 || bs < 32 || (bs & (bs - 1))) return false;
+  const GemmOps o = gemm_ops(act_dtype, scale_dtype, has_zp);
+  int a, b, c;
+  return gemm_plan(kModeDN, o.ws, false, K / bs, has_zp, a, b, c);
+}
+
+bool prefill_fits(int H, int I, int bs, int act_dtype, int scale_dtype, bool has_zp_gu, bool has_zp_d) {
   if (H % 128 || I % 64 || bs < 32 || (bs & (bs - 1))) return false;
   int a, b, c;
-  return gemm_plan(kModeGU, split, H / bs, has_zp_gu, a, b, c) && gemm_plan(kModeDN, split, I / bs, has_zp_d, a, b, c);
+  return gemm_plan(kModeGU, gemm_ops(act_dtype, scale_dtype, has_zp_gu).ws, false, H / bs, has_zp_gu, a, b, c) &&
+         gemm_plan(kModeDN, gemm_ops(act_dtype, scale_dtype, has_zp_d).ws, true, I / bs, has_zp_d, a, b, c);
 }
+
+bool prefill_x_to_f16(int act_dtype, int scale_dtype) { return scale_dtype == 1 && act_dtype == 1; }
 
 cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int, cudaStream_t st, bool pdl) {
   const int A = p.T * p.k;
@@ -724,59 +788,67 @@ cudaError_t launch_prefill_permute(const PrefillParams& p, const void* x, int, c
   return launch_kernel(permute_kernel, dim3(blocks), dim3(256), 0, st, pdl, static_cast<const uint16_t*>(x), p);
 }
 
-template <int MODE, typename TA, typename TS, bool Z, bool SPLIT>
+template <int MODE, typename OT, typename TS, bool Z, bool WS, bool AS>
 static cudaError_t launch_gemm_t(PrefillParams p, const CUtensorMap* m, cudaStream_t st, bool pdl) {
   const int K = (MODE == kModeGU) ? p.H : p.I;
-  if (!gemm_plan(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz, p.npk)) return cudaErrorInvalidValue;
-  const GemmSmem L = gemm_smem(MODE, SPLIT, K / p.bs, Z, p.nst, p.nsz, p.npk);
-  auto fn = gemm_kernel<MODE, TA, TS, Z, SPLIT>;
+  constexpr bool BLO = AS && MODE == kModeDN;
+  if (!gemm_plan(MODE, WS, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk)) return cudaErrorInvalidValue;
+  const GemmSmem L = gemm_smem(MODE, WS, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk);
+  auto fn = gemm_kernel<MODE, OT, TS, Z, WS, AS>;
   cudaError_t err = ensure_smem(fn, L.total);
   if (err != cudaSuccess) return err;
   return launch_kernel(fn, dim3(device_sm_count()), dim3(kGemmThreads), (size_t)L.total, st, pdl, m[0], m[1], m[2],
                        m[3], p);
 }
 
-template <int MODE, typename TA, typename TS>
-static cudaError_t dispatch_zs(const PrefillParams& p, bool z, bool split, const CUtensorMap* m, cudaStream_t st,
-                               bool pdl) {
-  if (split) return z ? launch_gemm_t<MODE, TA, TS, true, true>(p, m, st, pdl)
-                      : launch_gemm_t<MODE, TA, TS, false, true>(p, m, st, pdl);
-  return z ? launch_gemm_t<MODE, TA, TS, true, false>(p, m, st, pdl)
-           : launch_gemm_t<MODE, TA, TS, false, false>(p, m, st, pdl);
+// (operand type, weight split) follow from the dtypes and zero points
+// (gemm_ops); AS: the down GEMM of the layer takes the SwiGLU output as
+// hi + lo, the dense MatMulNBits takes x alone
+template <int MODE, typename TS>
+static cudaError_t dispatch_gemm_ts(const PrefillParams& p, bool f16, bool z, bool as, const CUtensorMap* m,
+                                    cudaStream_t st, bool pdl) {
+#define QMOE_G(OT, Z_, WS_) return as ? launch_gemm_t<MODE, OT, TS, Z_, WS_, true>(p, m, st, pdl) \
+                                      : launch_gemm_t<MODE, OT, TS, Z_, WS_, false>(p, m, st, pdl)
+  if (std::is_same<TS, __nv_bfloat16>::value) {  // fp16 operands; one weight operand without zero points
+    if (z) QMOE_G(__half, true, true);
+    QMOE_G(__half, false, false);
+  }
+  if (f16) {
+    if (z) QMOE_G(__half, true, true);
+    QMOE_G(__half, false, true);
+  }
+  if (z) QMOE_G(__nv_bfloat16, true, true);
+  QMOE_G(__nv_bfloat16, false, true);
+#undef QMOE_G
 }
 
-template <int MODE>
-static cudaError_t dispatch_gemm(const PrefillParams& p, int act_dtype, int scale_dtype, bool z, bool split,
-                                 const CUtensorMap* m, cudaStream_t st, bool pdl) {
-  if (act_dtype == 1)
-    return scale_dtype == 1 ? dispatch_zs<MODE, __nv_bfloat16, __nv_bfloat16>(p, z, split, m, st, pdl)
-                            : dispatch_zs<MODE, __nv_bfloat16, __half>(p, z, split, m, st, pdl);
-  return scale_dtype == 1 ? dispatch_zs<MODE, __half, __nv_bfloat16>(p, z, split, m, st, pdl)
-                          : dispatch_zs<MODE, __half, __half>(p, z, split, m, st, pdl);
-}
-
-cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype, int scale_dtype, bool split,
+cudaError_t launch_prefill_gemm(const PrefillParams& p, int mode, int act_dtype, int scale_dtype, bool dense,
                                 cudaStream_t st, bool pdl) {
   const int A = p.T * p.k;
-  const CUtensorMapDataType adt = act_dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const GemmOps o = gemm_ops(act_dtype, scale_dtype, false);
+  const CUtensorMapDataType odt = o.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap m[4];
   if (mode == kModeGU) {
     if (!make_map(&m[0], p.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.H / 2, (uint64_t)p.E * p.I, 32, 64,
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&m[1], p.w[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.H / 2, (uint64_t)p.E * p.I, 32, 64,
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&m[2], p.xp, adt, 2, p.H, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&m[2], p.xp, odt, 2, p.H, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorNotSupported;
     m[3] = m[2];
-    return dispatch_gemm<kModeGU>(p, act_dtype, scale_dtype, p.z[0] != nullptr, split, m, st, pdl);
+    return scale_dtype == 1
+               ? dispatch_gemm_ts<kModeGU, __nv_bfloat16>(p, o.f16, p.z[0] != nullptr, false, m, st, pdl)
+               : dispatch_gemm_ts<kModeGU, __half>(p, o.f16, p.z[0] != nullptr, false, m, st, pdl);
   }
+  const bool as = !dense;
   if (!make_map(&m[0], p.w[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.I / 2, (uint64_t)p.E * p.H, 32, 128,
                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map(&m[2], p.act, adt, 2, p.I, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m[3], split ? p.act_lo : p.act, adt, 2, p.I, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&m[2], p.act, odt, 2, p.I, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[3], as ? p.act_lo : p.act, odt, 2, p.I, A, 64, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorNotSupported;
   m[1] = m[0];
-  return dispatch_gemm<kModeDN>(p, act_dtype, scale_dtype, p.z[2] != nullptr, split, m, st, pdl);
+  return scale_dtype == 1 ? dispatch_gemm_ts<kModeDN, __nv_bfloat16>(p, o.f16, p.z[2] != nullptr, as, m, st, pdl)
+                          : dispatch_gemm_ts<kModeDN, __half>(p, o.f16, p.z[2] != nullptr, as, m, st, pdl);
 }
 
 cudaError_t launch_dense_setup(const PrefillParams& p, const void* x, cudaStream_t st, bool pdl) {

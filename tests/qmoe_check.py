@@ -95,3 +95,63 @@ def run_layer_and_check(wl, L, path, accumulate=False, seed=0):
     if accumulate:
         ref = ref + out0.double().cpu().numpy()
     return o, tw, ti, assert_close_layer(o, ref, wl.name), int(near.sum())
+
+
+# ---- the oracle over many tokens, spread over the host's cores.  Each
+# token's output depends only on that token, so token chunks are independent
+# oracle calls.  Workers start by spawn (the test process already holds a
+# CUDA context) and memory-map the layer's tensors from a temporary folder.
+_TENSORS = ("x", "router_w", "router_bias", "gate_w", "gate_s", "gate_zp", "up_w", "up_s", "up_zp",
+            "down_w", "down_s", "down_zp")
+_INTS = ("T", "H", "I", "E", "k", "block_size", "act_dtype", "scale_dtype")
+
+
+def _oracle_chunk(args):
+    import os as _os
+    import numpy as _np
+    import oracle as _oracle
+    folder, lo, hi, ints, present = args
+    L = dict(ints)
+    for n in present:
+        a = _np.load(_os.path.join(folder, n + ".npy"), mmap_mode="r")
+        L[n] = a[lo:hi] if n == "x" else a
+    L["T"] = hi - lo
+    out, ids, w, probs = _oracle.qmoe_forward(L)
+    return lo, out, ids, w, probs
+
+
+def oracle_forward_parallel(L, nproc=None):
+    """oracle.qmoe_forward(L) over all of L's tokens, one contiguous chunk per
+    process (each oracle call copies the whole layer's weights once, so
+    fewer, larger chunks are faster).  Returns (out, ids, w, probs) like
+    oracle.qmoe_forward."""
+    import multiprocessing as mp
+    import os
+    import shutil
+    import tempfile
+    folder = tempfile.mkdtemp(prefix="qmoe_oracle_")
+    try:
+        present = []
+        for n in _TENSORS:
+            t = L.get(n)
+            if t is None:
+                continue
+            if isinstance(t, torch.Tensor):
+                t = t.detach().cpu().contiguous()
+                if t.dtype in (torch.float16, torch.bfloat16):
+                    t = t.view(torch.int16)
+                t = t.numpy()
+            np.save(os.path.join(folder, n + ".npy"), np.ascontiguousarray(t))
+            present.append(n)
+        ints = {n: int(L[n]) for n in _INTS}
+        T = ints["T"]
+        nproc = max(1, min(T, nproc or os.cpu_count() or 1))
+        chunk = -(-T // nproc)
+        jobs = [(folder, lo, min(T, lo + chunk), ints, present) for lo in range(0, T, chunk)]
+        with mp.get_context("spawn").Pool(nproc) as pool:
+            parts = pool.map(_oracle_chunk, jobs)
+        parts.sort(key=lambda r: r[0])
+        return (np.concatenate([p[1] for p in parts]), np.concatenate([p[2] for p in parts]),
+                np.concatenate([p[3] for p in parts]), np.concatenate([p[4] for p in parts]))
+    finally:
+        shutil.rmtree(folder, ignore_errors=True)
