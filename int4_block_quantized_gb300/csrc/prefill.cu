@@ -18,19 +18,19 @@
 //   a weight producer streams packed int4 tiles (TMA) and each tile's block
 //           scales / zero points (bulk copies) through a deep ring;
 //   a token producer streams token tiles (TMA, 128-byte swizzle);
-//   eight dequantiser warps turn the codes into exact hi + lo operands in
-//           the canonical 128-byte-swizzled K-major layout;
-//   one thread issues tcgen05.mma into a double-buffered TMEM accumulator;
+//   eight dequantiser warps turn the codes into exact operands in
+//           registers and store them into tensor memory (tcgen05.st): the
+//           MMA reads the weight operand from TMEM, so shared memory only
+//           carries the codes and the token tiles;
+//   one thread issues tcgen05.mma (A from TMEM, B from shared memory) into
+//           a double-buffered TMEM accumulator;
 //   four epilogue warps tcgen05.ld it and apply SwiGLU or the weighted
 //           fp32 scatter-add.
-// Operands are exact.  With bf16 block scales a dequantised weight w = (q -
-// zp) * s has at most 12 significant bits and enters as one fp16 operand
-// (the activations converted to fp16 as well, exactly in fp16's range);
-// with fp16 scales it has up to 15 and enters as hi = RN(w) plus lo = w - hi
-// in the activation dtype.  The SwiGLU output enters the down GEMM as
-// hi + lo likewise.  K is permuted inside every group of 8 (order
-// 0,4,1,5,2,6,3,7) identically for weights and activations so one LOP3
-// yields two operands from a 32-bit word.
+// Operands are exact (the rule is stated at gemm_ops below): a dequantised
+// weight enters as one fp16 operand or as hi = RN(w) plus lo = w - hi; the
+// SwiGLU output enters the down GEMM as hi + lo.  K is permuted inside every
+// group of 8 (order 0,4,1,5,2,6,3,7) identically for weights and
+// activations so one LOP3 yields two operands from a 32-bit word.
 #include <cuda.h>
 #include <math.h>
 
@@ -297,38 +297,39 @@ __device__ __forceinline__ void split_act(float a, uint16_t& h, uint16_t& l) {
 }
 
 // ------------------------------------------------------------ grouped GEMM
-constexpr uint32_t kTileOp = 128 * 128;    // 16-bit operand tile: 128 rows x 64 K (SW128)
+constexpr uint32_t kTileOp = 128 * 128;    // 16-bit token tile: 128 rows x 64 K (SW128)
 constexpr uint32_t kPkBytes = 128 * 32;    // packed codes: 128 rows x 64 codes
 constexpr int kMaxPk = 24;                 // packed-code ring slots (at most)
+constexpr int kMaxSt = 4;                  // operand stages (at most)
 constexpr uint32_t kGbufFloats = 64 * 17;  // gate values of one 16-column chunk (padded rows)
-constexpr uint32_t kTmemCols = 256;        // two 128-column accumulators
+constexpr uint32_t kTmemCols = 512;        // the whole TMEM of the SM (one CTA per SM)
+constexpr uint32_t kAccCols = 2 * kBN;     // two 128-column accumulators, then the weight stages
 constexpr uint32_t kSmemLimit = 232448;    // 227 KB per CTA
-constexpr int kDeqWarps = 8;               // two per SM sub-partition: row = warp%4*32+lane, half = K half
+constexpr uint32_t kNapNs = 256;          // poll interval of the off-critical-path waits
+constexpr uint32_t kMmaNapNs = 32;        // poll interval of the MMA issuer's waits (see the issuer)
+constexpr int kDeqWarps = 8;               // two per sub-partition: row = warp%4*32+lane, half = warp/4
 
-// Warp roles (kGemmThreads = 512; warp w issues from SM sub-partition w % 4):
-//   1      TMEM owner and tcgen05.mma issuer
-//   5      token-tile producer (TMA, L2-resident gathered tokens / SwiGLU output)
-//   9      weight producer: packed codes (deep ring) and each tile's scales / zero points
-//   0,4,8,2,6,10,3,7  dequantisers (row quadrant = index % 4, K half = index / 4)
+// Warp roles (kGemmThreads = 512; warp w issues from SM sub-partition w % 4
+// and may touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31):
+//   0-7    dequantisers (TMEM lane quadrant = warp % 4, K half = warp / 4)
+//   8      TMEM owner and tcgen05.mma issuer (converged warp, elected lane)
+//   9      token-tile producer (TMA, L2-resident gathered tokens / SwiGLU output)
+//   10     weight producer: packed codes (deep ring) and each tile's scales / zero points
 //   11     idle
 //   12-15  epilogue (TMEM lane quadrant = warp % 4)
-// The three issuing roles share sub-partition 1: measured on GB300, a
-// dequantiser sharing a sub-partition with the MMA issuer or a TMA issuer
-// fell 900-1650 cycles behind the others on every 64-wide K chunk.
-// Shared memory: [barriers][scale buffers][operand stages: A hi, A lo, B hi, B lo][packed ring][exchange]
+// TMEM columns: [0, 256) the two accumulators; from 256 one weight operand
+// stage per 64-wide K chunk: 32 columns (64 16-bit values per row), twice
+// that with hi + lo.
+// Shared memory: [barriers][scale buffers][token stages: B hi, B lo][packed ring][exchange]
 struct GemmSmem {
-  uint32_t a_lo, b_hi, b_lo, stage;  // offsets inside an operand stage, stage size
+  uint32_t b_lo, stage;  // offset of the low tile inside a token stage, stage size
   uint32_t sz_bytes, sz_off, stage_off, pk_off, gbuf_off, total;
 };
-// ws: weights as hi + lo operands; as: activations (down: SwiGLU output) as hi + lo
-__host__ __device__ inline GemmSmem gemm_smem(int mode, bool ws, bool as, int nb, bool has_zp, int nst, int nsz,
-                                              int npk) {
+// as: activations (down: SwiGLU output) as hi + lo
+__host__ __device__ inline GemmSmem gemm_smem(int mode, bool as, int nb, bool has_zp, int nst, int nsz, int npk) {
   GemmSmem S;
-  const uint32_t na = ws ? 2 : 1, nbt = as ? 2 : 1;
-  S.a_lo = kTileOp;
-  S.b_hi = na * kTileOp;
-  S.b_lo = S.b_hi + kTileOp;
-  S.stage = S.b_hi + nbt * kTileOp;
+  S.b_lo = kTileOp;
+  S.stage = (as ? 2u : 1u) * kTileOp;
   S.sz_bytes = ((uint32_t)128 * nb * 2 + (has_zp ? (uint32_t)128 * nb : 0u) + 1023u) & ~1023u;
   S.sz_off = 1024;
   S.stage_off = S.sz_off + nsz * S.sz_bytes;
@@ -339,16 +340,17 @@ __host__ __device__ inline GemmSmem gemm_smem(int mode, bool ws, bool as, int nb
 }
 // Pipeline plan.  Two tile-scale buffers first (with one, the weight
 // producer cannot start the next tile's codes until the current tile is
-// dequantised), then 3 operand stages if at least 8 packed slots remain,
-// else 2; the packed ring takes the rest (<= 24 slots).  Long reductions
-// with small blocks (large whole-K scale buffers) fall back to one scale
-// buffer and as few as 4 packed slots.
-__host__ inline bool gemm_plan(int mode, bool ws, bool as, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
+// dequantised), then 4 operand stages down to 2 while at least 12 packed
+// slots remain; the packed ring takes the rest (<= 24 slots).  Long
+// reductions with small blocks (large whole-K scale buffers) fall back to
+// one scale buffer and as few as 4 packed slots.  Four stages fit TMEM with
+// hi + lo weights (4 x 64 columns after the accumulators).
+__host__ inline bool gemm_plan(int mode, bool as, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
   for (int sz = 2; sz >= 1; --sz)
-    for (int st = 3; st >= 2; --st) {
-      const int pmin = sz == 1 && st == 2 ? 4 : 8;
+    for (int st = kMaxSt; st >= 2; --st) {
+      const int pmin = sz == 1 && st == 2 ? 4 : 12;
       int pk = kMaxPk;
-      while (pk >= pmin && gemm_smem(mode, ws, as, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
+      while (pk >= pmin && gemm_smem(mode, as, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
       if (pk >= pmin) {
         nst = st;
         nsz = sz;
@@ -359,14 +361,17 @@ __host__ inline bool gemm_plan(int mode, bool ws, bool as, int nb, bool has_zp, 
   return false;
 }
 
-// bounded wait that also gives up once another role has aborted
+// bounded wait that also gives up once another role has aborted.  nap_ns >
+// 0 (roles whose waits are long and off the critical path: the producers
+// and the epilogue's wait for a finished accumulator) sleeps between polls,
+// so that the waiting warps leave the issue slots to the dequantisers and
+// the MMA issuer; the others poll with try_wait's own suspend hint.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                              volatile int* abort) {
+                                              volatile int* abort, uint32_t nap_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  // suspended between checks, so that waiting roles leave the issue slots
-  // to the dequantising warps
-  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+  while (!(nap_ns ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u))) {
+    if (nap_ns) __nanosleep(nap_ns);
     if (*abort) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       set_status(status, QMOE_ST_TIMEOUT);
@@ -399,26 +404,31 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int n, int issued) {
 // One persistent CTA per SM.  Work item t = (weight row block mb, token
 // tile nt), nt fastest, so the token tiles of one expert run side by side
 // and share the weight tile through L2.
-// OT: operand type (fp16 / bf16); WS / AS as for gemm_smem
+// OT: operand type (fp16 / bf16); WS: weights as hi + lo; AS: activations
+// (down: the SwiGLU output) as hi + lo
 template <int MODE, typename OT, typename TS, bool HAS_ZP, bool WS, bool AS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                 const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
                 const PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // 1024-byte aligned start (128-byte swizzle), reached by pointer arithmetic
+  // on the shared array so every access below compiles to a shared-memory
+  // instruction rather than a generic one
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   constexpr bool GU = MODE == kModeGU;
   constexpr bool BLO = AS && !GU;  // second B tile (activation low part)
   const int K = GU ? p.H : p.I;       // reduction length
   const int NR = GU ? p.I : p.H;      // weight rows per expert matrix
   const int nb = K >> p.lbs;
   const int nst = p.nst, nsz = p.nsz, npk = p.npk;
-  const GemmSmem L = gemm_smem(MODE, WS, BLO, nb, HAS_ZP, nst, nsz, npk);
+  const GemmSmem L = gemm_smem(MODE, BLO, nb, HAS_ZP, nst, nsz, npk);
+  constexpr uint32_t AW = WS ? 64 : 32;  // TMEM columns of one weight operand stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* b_full = bars;                  // [4] token tile landed
-  uint64_t* a_full = bars + 4;              // [4] operand dequantised (one arrival per dequant warp)
-  uint64_t* empty = bars + 8;               // [4] MMAs done with the operand stage
-  uint64_t* pk_full = bars + 12;            // [kMaxPk] packed codes landed
+  uint64_t* b_full = bars;                  // [kMaxSt] token tile landed
+  uint64_t* a_full = bars + kMaxSt;         // [kMaxSt] weights in TMEM (one arrival per dequant warp)
+  uint64_t* empty = bars + 2 * kMaxSt;      // [kMaxSt] MMAs done with the stage
+  uint64_t* pk_full = bars + 3 * kMaxSt;    // [kMaxPk] packed codes landed
   uint64_t* pk_empty = pk_full + kMaxPk;    // [kMaxPk] packed codes read
   uint64_t* tmem_full = pk_empty + kMaxPk;  // [2] accumulator complete
   uint64_t* tmem_empty = tmem_full + 2;     // [2] accumulator drained
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int MB = NR / (GU ? 64 : 128);
 
   if (tid == 0) {
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < kMaxSt; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&a_full[s], kDeqWarps);
       mbar_init(&empty[s], 1);
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == 8) {
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
@@ -469,16 +479,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  // dequantiser index of this warp (-1: another role)
-  const int deq = warp == 0 ? 0 : warp == 4 ? 1 : warp == 8 ? 2 : warp == 2 ? 3 : warp == 6 ? 4 : warp == 10 ? 5
-                : warp == 3 ? 6 : warp == 7 ? 7 : -1;
   pdl_wait();  // routing, token tiles and (down) the SwiGLU output come from earlier grids
   pdl_trigger();
   const int NT = (int)__ldcg(p.ctl + kCtlNtiles);
   const int ntile_total = NT * MB;
   const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
 
-  if (warp == 5) {
+  if (warp == 9) {
     // ============================================================ token-tile producer
     if (lane == 0) {
       int it = 0;
@@ -489,19 +496,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int nbox = (npad + kBoxRows - 1) / kBoxRows;
         const uint32_t btx = nbox * kBoxRows * 128 * (BLO ? 2 : 1);
         for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst)) {
-          if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) break;
+          if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort, kNapNs)) break;
           uint8_t* st = stages + rs.i * L.stage;
           uint64_t* fb = &b_full[rs.i];
           mbar_arrive_expect_tx(fb, btx);
           for (int bx = 0; bx < nbox; ++bx) {
-            tma_load_2d(st + L.b_hi + bx * kBoxRows * 128, &tm_b, kc * 64, row0 + bx * kBoxRows, fb);
+            tma_load_2d(st + bx * kBoxRows * 128, &tm_b, kc * 64, row0 + bx * kBoxRows, fb);
             if (BLO) tma_load_2d(st + L.b_lo + bx * kBoxRows * 128, &tm_b2, kc * 64, row0 + bx * kBoxRows, fb);
           }
         }
       }
       if (*s_abort) drain_ring(b_full, nst, it);
     }
-  } else if (warp == 9) {
+  } else if (warp == 10) {
     // ============================================================ weight producer
     if (lane == 0) {
       int ip = 0, tc = 0;
@@ -510,7 +517,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = blockIdx.x; t < ntile_total && !*s_abort; t += gridDim.x, ++tc, rz.next(nsz)) {
         const int4 tl = __ldcg(tiles + t % NT);
         const int mb = t / NT, e = tl.x;
-        if (tc >= nsz && !wait_or_abort(&sz_empty[rz.i], rz.ph ^ 1u, status, s_abort)) break;
+        if (tc >= nsz && !wait_or_abort(&sz_empty[rz.i], rz.ph ^ 1u, status, s_abort, kNapNs)) break;
         // block scales / zero points of the tile's 128 weight rows over the whole K
         uint8_t* sz = szbuf + rz.i * L.sz_bytes;
         uint64_t* zb = &sz_full[rz.i];
@@ -529,7 +536,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (HAS_ZP) bulk_g2s(sz + sbytes, p.z[2] + r * nb, zbytes, zb);
         }
         for (int kc = 0; kc < KC; ++kc, ++ip, rp.next(npk)) {
-          if (ip >= npk && !wait_or_abort(&pk_empty[rp.i], rp.ph ^ 1u, status, s_abort)) break;
+          if (ip >= npk && !wait_or_abort(&pk_empty[rp.i], rp.ph ^ 1u, status, s_abort, kNapNs)) break;
           uint8_t* pk = pkbuf + rp.i * kPkBytes;
           uint64_t* fb = &pk_full[rp.i];
           mbar_arrive_expect_tx(fb, kPkBytes);
@@ -546,55 +553,67 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         drain_ring(sz_full, nsz, tc);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 8) {
     // ============================================================ MMA issuer
-    if (lane == 0) {
-      int tc = 0;
-      bool issued = false;
-      Ring rs;
-      constexpr bool bf = std::is_same<OT, __nv_bfloat16>::value;
-      for (int t = blockIdx.x; t < ntile_total; t += gridDim.x, ++tc) {
-        const int4 tl = __ldcg(tiles + t % NT);
-        const uint32_t idesc = idesc_f16(128, (tl.z + 15) & ~15, bf);
-        const int b = tc & 1;
-        if (tc >= 2 && !wait_or_abort(&tmem_empty[b], ((tc >> 1) - 1) & 1, status, s_abort)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * kBN;
-        bool ok = true;
-        for (int kc = 0; kc < KC; ++kc, rs.next(nst)) {
-          if (!wait_or_abort(&a_full[rs.i], rs.ph, status, s_abort) ||
-              !wait_or_abort(&b_full[rs.i], rs.ph, status, s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t st = smem_u32(stages + rs.i * L.stage);
-          const uint64_t ah = sw128_desc(st), al = sw128_desc(st + L.a_lo);
-          const uint64_t bh = sw128_desc(st + L.b_hi), bl = sw128_desc(st + L.b_lo);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // K = 16 per instruction: +32 bytes in the swizzled row
-            mma_f16_ss(d_tmem, ah + 2 * kk, bh + 2 * kk, idesc, (kc | kk) != 0);
-            if (WS) mma_f16_ss(d_tmem, al + 2 * kk, bh + 2 * kk, idesc, 1u);
-            if (BLO) mma_f16_ss(d_tmem, ah + 2 * kk, bl + 2 * kk, idesc, 1u);
-          }
-          issued = true;
-          mma_commit(&empty[rs.i]);
+    // The whole warp runs the loop and one elected lane issues: a lone
+    // active lane of a diverged warp issues tcgen05.mma at half the rate.
+    int tc = 0;
+    bool issued = false;
+    Ring rs;
+    constexpr bool bf = std::is_same<OT, __nv_bfloat16>::value;
+    for (int t = blockIdx.x; t < ntile_total; t += gridDim.x, ++tc) {
+      const int4 tl = __ldcg(tiles + t % NT);
+      const uint32_t idesc = idesc_f16(128, (tl.z + 15) & ~15, bf);
+      const int b = tc & 1;
+      if (tc >= 2 && !wait_or_abort(&tmem_empty[b], ((tc >> 1) - 1) & 1, status, s_abort)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + b * kBN;
+      bool ok = true;
+      for (int kc = 0; kc < KC; ++kc, rs.next(nst)) {
+        if (!wait_or_abort(&a_full[rs.i], rs.ph, status, s_abort, kMmaNapNs) ||
+            !wait_or_abort(&b_full[rs.i], rs.ph, status, s_abort, kMmaNapNs)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        mma_commit(&tmem_full[b]);
+        tc_fence_after();
+        const uint32_t st = smem_u32(stages + rs.i * L.stage);
+        const uint64_t bh = sw128_desc(st), bl = sw128_desc(st + L.b_lo);
+        const uint32_t ah = tmem_base + kAccCols + rs.i * AW, al = ah + 32;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // K = 16 per instruction: 8 TMEM columns, +32 bytes in the swizzled row
+          mma_f16_ts_elect(d_tmem, ah + 8 * kk, bh + 2 * kk, idesc, (kc | kk) != 0);
+          if (WS) mma_f16_ts_elect(d_tmem, al + 8 * kk, bh + 2 * kk, idesc, 1u);
+          if (BLO) mma_f16_ts_elect(d_tmem, ah + 8 * kk, bl + 2 * kk, idesc, 1u);
+        }
+        issued = true;
+        mma_commit_elect(&empty[rs.i]);
       }
-      if (*s_abort && issued) {  // MMAs still in flight must finish before TMEM is freed
-        mma_commit(fin);
-        mbar_wait(fin, 0, nullptr);
-      }
+      if (!ok) break;
+      mma_commit_elect(&tmem_full[b]);
     }
-  } else if (deq >= 0) {
+    if (*s_abort && issued) {  // MMAs still in flight must finish before TMEM is freed
+      mma_commit_elect(fin);
+      mbar_wait(fin, 0, nullptr);
+    }
+  } else if (warp < kDeqWarps) {
     // ============================================================ dequantisers
-    const int r = (deq & 3) * 32 + lane;  // weight row of the tile
-    const int hh = deq >> 2;              // which 32 codes of the 64-wide chunk
+    const int qd = warp & 3;              // TMEM lane quadrant of this warp
+    const int r = qd * 32 + lane;         // weight row of the tile
+    const int hh = warp >> 2;             // which 32 codes of the 64-wide chunk
+    const uint32_t a_row = tmem_base + ((uint32_t)(qd * 32) << 16) + kAccCols + hh * 16;
+    const int nchunks = blockIdx.x < ntile_total ? ((ntile_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * KC : 0;
     int it = 0;
     Ring rs, rp, rz;
     bool ok = true;
+    // This chunk's codes are loaded one chunk ahead, so the shared-memory
+    // latency overlaps the previous chunk's work.
+    uint4 q = make_uint4(0, 0, 0, 0);
+    if (nchunks > 0) {
+      if (wait_or_abort(&pk_full[0], 0, status, s_abort))
+        q = *reinterpret_cast<const uint4*>(pkbuf + r * 32 + hh * 16);
+      else
+        ok = false;
+    }
     // The rows of a tile's scales sit nb * 2 bytes apart: at 128 bytes the 32
     // rows of a warp fall into one bank.  When rows are 16-byte aligned a
     // lane reads 8 consecutive block scales (and 8 zero points) at once and
@@ -609,8 +628,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint4 sv = make_uint4(0, 0, 0, 0);
       uint2 zv = make_uint2(0, 0);
       for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst), rp.next(npk)) {
-        if (!wait_or_abort(&pk_full[rp.i], rp.ph, status, s_abort)) { ok = false; break; }
-        const uint4 q = *reinterpret_cast<const uint4*>(pkbuf + rp.i * kPkBytes + r * 32 + hh * 16);
         // block_size >= 32: the 32 codes of this half share one block
         const int blk = (kc * 64 + hh * 32) >> p.lbs;
         uint32_t zpv;
@@ -631,35 +648,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         Deq<OT, TS> d;
         d.set(zpv, scv);
-        if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) { ok = false; break; }
-        uint8_t* st = stages + rs.i * L.stage;
-        const uint32_t roff = (r >> 3) * 1024 + (r & 7) * 128;
+        // column c of the row holds K elements 2c, 2c + 1 of the permuted
+        // order: group g's pairs (0,4), (1,5), (2,6), (3,7) in columns 4g..4g+3
+        uint32_t h[16], l[16];
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
-          const int g = hh * 4 + gg;
-          const uint32_t off = roff + ((g ^ (r & 7)) << 4);  // 128-byte swizzle
-          uint4 h, l;  // elements (0,4), (1,5), (2,6), (3,7) of the group
-          if (WS) {
-            d.both(w[gg], h.x, l.x);
-            d.both(w[gg] >> 4, h.y, l.y);
-            d.both(w[gg] >> 8, h.z, l.z);
-            d.both(w[gg] >> 12, h.w, l.w);
-            *reinterpret_cast<uint4*>(st + off) = h;
-            *reinterpret_cast<uint4*>(st + L.a_lo + off) = l;
-          } else {
-            h.x = d.hi(w[gg]);
-            h.y = d.hi(w[gg] >> 4);
-            h.z = d.hi(w[gg] >> 8);
-            h.w = d.hi(w[gg] >> 12);
-            *reinterpret_cast<uint4*>(st + off) = h;
+        for (int gg = 0; gg < 4; ++gg)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            if (WS)
+              d.both(w[gg] >> (4 * jj), h[gg * 4 + jj], l[gg * 4 + jj]);
+            else
+              h[gg * 4 + jj] = d.hi(w[gg] >> (4 * jj));
           }
+        if (it + 1 < nchunks) {  // the next chunk's codes (the next ring slot)
+          Ring rn = rp;
+          rn.next(npk);
+          if (!wait_or_abort(&pk_full[rn.i], rn.ph, status, s_abort)) { ok = false; break; }
+          q = *reinterpret_cast<const uint4*>(pkbuf + rn.i * kPkBytes + r * 32 + hh * 16);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ta = a_row + rs.i * AW;
+        tmem_st16(ta, h);
+        if (WS) tmem_st16(ta + 32, l);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
-        // the packed slot is handed back only once the operand it produced is
-        // written: releasing it right after the load let the next TMA fill
-        // race with this chunk on the GPU (wrong rows in a few tiles)
+        // the packed slot is handed back only once the operand it produced
+        // is stored: releasing it right after the load once let the next TMA
+        // fill race with the chunk (wrong rows in a few tiles)
         if (lane == 0) {
           mbar_arrive(&a_full[rs.i]);
           mbar_arrive(&pk_empty[rp.i]);
@@ -680,7 +698,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int mb = t / NT;
       const int row0 = tl.y, nrows = tl.z, npad = (nrows + 15) & ~15;
       const int b = tc & 1;
-      if (!wait_or_abort(&tmem_full[b], (tc >> 1) & 1, status, s_abort)) break;
+      if (!wait_or_abort(&tmem_full[b], (tc >> 1) & 1, status, s_abort, kNapNs)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
       for (int c0 = 0; c0 < npad; c0 += 16, ++cc) {
@@ -743,7 +761,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -768,16 +786,18 @@ static inline GemmOps gemm_ops(int act_dtype, int scale_dtype, bool has_zp) {
 
 bool dense_fits(int N, int K, int bs, int act_dtype, int scale_dtype, bool has_zp) {
   if (N % 128 || K % 64 || bs < 32 || (bs & (bs - 1))) return false;
-  const GemmOps o = gemm_ops(act_dtype, scale_dtype, has_zp);
+  (void)act_dtype;
+  (void)scale_dtype;
   int a, b, c;
-  return gemm_plan(kModeDN, o.ws, false, K / bs, has_zp, a, b, c);
+  return gemm_plan(kModeDN, false, K / bs, has_zp, a, b, c);
 }
 
 bool prefill_fits(int H, int I, int bs, int act_dtype, int scale_dtype, bool has_zp_gu, bool has_zp_d) {
   if (H % 128 || I % 64 || bs < 32 || (bs & (bs - 1))) return false;
+  (void)act_dtype;
+  (void)scale_dtype;
   int a, b, c;
-  return gemm_plan(kModeGU, gemm_ops(act_dtype, scale_dtype, has_zp_gu).ws, false, H / bs, has_zp_gu, a, b, c) &&
-         gemm_plan(kModeDN, gemm_ops(act_dtype, scale_dtype, has_zp_d).ws, true, I / bs, has_zp_d, a, b, c);
+  return gemm_plan(kModeGU, false, H / bs, has_zp_gu, a, b, c) && gemm_plan(kModeDN, true, I / bs, has_zp_d, a, b, c);
 }
 
 bool prefill_x_to_f16(int act_dtype, int scale_dtype) { return scale_dtype == 1 && act_dtype == 1; }
@@ -792,12 +812,15 @@ template <int MODE, typename OT, typename TS, bool Z, bool WS, bool AS>
 static cudaError_t launch_gemm_t(PrefillParams p, const CUtensorMap* m, cudaStream_t st, bool pdl) {
   const int K = (MODE == kModeGU) ? p.H : p.I;
   constexpr bool BLO = AS && MODE == kModeDN;
-  if (!gemm_plan(MODE, WS, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk)) return cudaErrorInvalidValue;
-  const GemmSmem L = gemm_smem(MODE, WS, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk);
+  if (!gemm_plan(MODE, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk)) return cudaErrorInvalidValue;
+  const GemmSmem L = gemm_smem(MODE, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk);
+  // the kernel takes all of the SM's TMEM: at least half the shared memory
+  // keeps a second CTA off the SM
+  const uint32_t smem = L.total > kSmemLimit / 2 + 1024 ? L.total : kSmemLimit / 2 + 1024;
   auto fn = gemm_kernel<MODE, OT, TS, Z, WS, AS>;
-  cudaError_t err = ensure_smem(fn, L.total);
+  cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(fn, dim3(device_sm_count()), dim3(kGemmThreads), (size_t)L.total, st, pdl, m[0], m[1], m[2],
+  return launch_kernel(fn, dim3(device_sm_count()), dim3(kGemmThreads), (size_t)smem, st, pdl, m[0], m[1], m[2],
                        m[3], p);
 }
 
