@@ -61,8 +61,15 @@ typedef enum {
   QMOE_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required     */
   QMOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed        */
   QMOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait ran out       */
-  QMOE_ERR_DEVICE_CHECK = 6  /* device status: an index check failed        */
+  QMOE_ERR_DEVICE_CHECK = 6  /* device status: an index or range check failed */
 } qmoe_status;
+
+/* Bits of a device status word (qmoe_get_device_status's *bits_out). */
+typedef enum {
+  QMOE_ST_TIMEOUT = 1, /* a bounded wait ran out                                 -> QMOE_ERR_TIMEOUT */
+  QMOE_ST_INDEX = 2,   /* an index check failed                                  -> QMOE_ERR_DEVICE_CHECK */
+  QMOE_ST_RANGE = 4    /* a value outside a format's or accumulator's range       -> QMOE_ERR_DEVICE_CHECK */
+} qmoe_status_bit;
 
 typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
 
@@ -145,6 +152,25 @@ size_t qmoe_workspace_size(int T, int H, int I, int E, int k);
  * again before the workspace's next use (a call that gave up part-way can
  * leave counters or the accumulator mid-update). */
 int qmoe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Diagnostics of the failure path, kept in the workspace's control block
+ * (qmoe_workspace_init clears both; callers otherwise leave them).
+ *   wait_limit_kilocycles  the grouped GEMM's bounded waits (prefill path and
+ *                          the tensor-core matmul_nbits_ex) give up after
+ *                          this many x 1024 SM cycles; 0: the default,
+ *                          about 2 s.
+ *   flags                  QMOE_DIAG_STALL_GEMM: the GEMM's dequantiser warps
+ *                          wait for a copy that cannot arrive, so that wait
+ *                          runs out; 0: none.
+ * A wait that gives up sets QMOE_ST_TIMEOUT; the kernel's roles then drain
+ * their copies and MMAs in flight, free TMEM and return (no trap, no hang);
+ * qmoe_get_device_status reports QMOE_ERR_TIMEOUT and that call's output is
+ * undefined.  The workspace stays usable: with the diagnostics cleared the
+ * next call computes normally.  Asynchronous on `stream` (an 8-byte copy
+ * into the control block).  QMOE_ERR_INVALID_ARG for unknown flags. */
+#define QMOE_DIAG_STALL_GEMM 1u
+int qmoe_workspace_set_diagnostics(void* workspace, size_t workspace_bytes, uint32_t wait_limit_kilocycles,
+                                   uint32_t flags, void* stream);
 
 /* Router: logits = x[T,H] . router_w[H,E] (+ router_bias[E]) accumulated in
  * fp32; softmax over all E in fp32; the k largest probabilities, best first,
@@ -314,17 +340,23 @@ int qmoe_rmsnorm(const void* x, void* out, int act_dtype, int T, int H, float ep
  *   scales  [E, K/bs, N]   16-bit (fp16 or bf16, copied bit for bit)
  * Output: w_out [E, N, K/2], scales_out [E, N, K/bs], zp_out [E, N, K/bs]
  * (NULL exactly when qzeros is NULL; the canonical layout then implies
- * zero point 8).  zp = min(stored + offset, 15): the offset is
- * *zero_offset_dev when that device pointer is given (for example the
- * output of qmoe_gptq_zero_offset, read by the kernel, so no host round
- * trip), else zero_offset (0 or 1).  Requires N a multiple of 8, K a
+ * zero point 8).  zp = stored + offset: the offset is *zero_offset_dev
+ * when that device pointer is given (for example the output of
+ * qmoe_gptq_zero_offset, read by the kernel, so no host round trip), else
+ * zero_offset (0 or 1).  A zero point of 16 (a stored 15 with offset 1)
+ * does not fit the canonical 4-bit zero point: it is written as 15 and, if
+ * status_dev (a 4-byte device word, may be NULL) is given, QMOE_ST_RANGE is
+ * OR-ed into it; read it with qmoe_get_device_status(status_dev, ...),
+ * which returns QMOE_ERR_DEVICE_CHECK when the bit is set.  The weights of
+ * such blocks differ from the checkpoint's by one scale step, so a caller
+ * should refuse the checkpoint.  Requires N a multiple of 8, K a
  * multiple of 32 and of block_size (32, 64, 128); 4-byte aligned int32
  * buffers and w_out, 2-byte aligned scales.  Asynchronous on `stream`;
  * input and output must not overlap.  Bound by HBM (every byte read and
  * written once). */
 int qmoe_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int E, int K,
                      int N, int block_size, int zero_offset, const int32_t* zero_offset_dev,
-                     uint8_t* w_out, void* scales_out, uint8_t* zp_out, void* stream);
+                     uint8_t* w_out, void* scales_out, uint8_t* zp_out, uint32_t* status_dev, void* stream);
 
 /* The GPTQ zero-point offset of a qzeros tensor (n_words int32 words, all
  * experts and projections the caller wants to judge together), written to
@@ -341,8 +373,11 @@ int qmoe_gptq_zero_offset(const int32_t* qzeros, size_t n_words, int32_t* offset
 int qmoe_unpack_zero_points(const uint8_t* zp_packed, int rows, int nb, uint8_t* zp_out, void* stream);
 
 /* Read (blocking: synchronises `stream`) and clear the device status word
- * of `workspace`.  Returns QMOE_OK, or the first QMOE_ERR_* recorded by a
- * kernel since the last read; *bits_out (may be NULL) gets the raw bits. */
+ * of `workspace` (its first 4 bytes; also any 4-byte status word such as
+ * qmoe_repack_gptq's status_dev).  Returns QMOE_OK, or QMOE_ERR_TIMEOUT
+ * if a wait ran out, else QMOE_ERR_DEVICE_CHECK if an index or range check
+ * failed since the last read; *bits_out (may be NULL) gets the raw bits
+ * (QMOE_ST_*). */
 int qmoe_get_device_status(void* workspace, uint32_t* bits_out, void* stream);
 
 #ifdef __cplusplus

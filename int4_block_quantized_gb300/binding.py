@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libqmoe.so")
 F16, BF16 = 0, 1
 PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_DECODE_SPLIT, PATH_DECODE_FUSED = 0, 1, 2, 4, 5
 DECODE_MAX_TOKENS = 16
+DIAG_STALL_GEMM = 1
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported device or shape",
            3: "workspace missing or too small", 4: "CUDA runtime error",
            5: "device wait timed out", 6: "device index check failed"}
@@ -51,6 +52,8 @@ def lib():
         L.qmoe_workspace_size.argtypes = [i32] * 5
         L.qmoe_workspace_init.restype = i32
         L.qmoe_workspace_init.argtypes = [vp, sz, vp]
+        L.qmoe_workspace_set_diagnostics.restype = i32
+        L.qmoe_workspace_set_diagnostics.argtypes = [vp, sz, ctypes.c_uint32, ctypes.c_uint32, vp]
         L.qmoe_route.restype = i32
         L.qmoe_route.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.matmul_nbits.restype = i32
@@ -81,7 +84,7 @@ def lib():
         L.qmoe_rmsnorm.restype = i32
         L.qmoe_rmsnorm.argtypes = [vp, vp, i32, i32, i32, ctypes.c_float, vp]
         L.qmoe_repack_gptq.restype = i32
-        L.qmoe_repack_gptq.argtypes = [vp, vp, vp] + [i32] * 5 + [vp, vp, vp, vp, vp]
+        L.qmoe_repack_gptq.argtypes = [vp, vp, vp] + [i32] * 5 + [vp, vp, vp, vp, vp, vp]
         L.qmoe_gptq_zero_offset.restype = i32
         L.qmoe_gptq_zero_offset.argtypes = [vp, sz, vp, vp]
         L.qmoe_unpack_zero_points.restype = i32
@@ -130,6 +133,14 @@ class Workspace:
     @property
     def ptr(self):
         return ctypes.c_void_p(self.buf.data_ptr())
+
+    def set_diagnostics(self, wait_limit_kilocycles=0, flags=0):
+        """Diagnostics of the failure path: the grouped GEMM's waits give up
+        after wait_limit_kilocycles x 1024 SM cycles (0: about 2 s); flags
+        DIAG_STALL_GEMM makes its dequantisers wait for a copy that cannot
+        arrive.  (0, 0) restores normal operation."""
+        _check(lib().qmoe_workspace_set_diagnostics(self.ptr, self.nbytes, int(wait_limit_kilocycles), int(flags),
+                                                    _stream()), "qmoe_workspace_set_diagnostics")
 
     def status(self):
         bits = ctypes.c_uint32(0)
@@ -299,18 +310,26 @@ def qmoe_gptq_zero_offset(qzeros):
     return off
 
 
-def qmoe_repack_gptq(qweight, qzeros, scales, block_size, zero_offset=0, zero_offset_dev=None):
+def qmoe_repack_gptq(qweight, qzeros, scales, block_size, zero_offset=0, zero_offset_dev=None, check=True,
+                     status=None):
     """GPTQ (qweight [E, K/8, N] int32, qzeros [E, K/bs, N/8] int32 or None,
     scales [E, K/bs, N]) -> canonical (w [E, N, K/2] u8, scales [E, N, K/bs],
-    zp [E, N, K/bs] u8 or None)."""
+    zp [E, N, K/bs] u8 or None).  A zero point above 15 (stored 15 with
+    offset 1) sets QMOE_ST_RANGE in the status word: with check=True (the
+    default) this synchronises and raises QMoEError; with check=False the
+    caller's own int32 device tensor `status` (if given) collects the bit."""
     E, K8, N = qweight.shape
     K = 8 * K8
     nb = K // block_size
     w = torch.empty((E, N, K // 2), dtype=torch.uint8, device=qweight.device)
     s = torch.empty((E, N, nb), dtype=scales.dtype, device=qweight.device)
     zp = torch.empty((E, N, nb), dtype=torch.uint8, device=qweight.device) if qzeros is not None else None
+    st = status if status is not None else (torch.zeros(1, dtype=torch.int32, device=qweight.device) if check else None)
     _check(lib().qmoe_repack_gptq(_p(qweight), _p(qzeros), _p(scales), E, K, N, block_size, int(zero_offset),
-                                  _p(zero_offset_dev), _p(w), _p(s), _p(zp), _stream()), "qmoe_repack_gptq")
+                                  _p(zero_offset_dev), _p(w), _p(s), _p(zp), _p(st), _stream()), "qmoe_repack_gptq")
+    if check and status is None:
+        _check(lib().qmoe_get_device_status(_p(st), None, _stream()),
+               "qmoe_repack_gptq (a GPTQ zero point above 15 does not fit the 4-bit format)")
     return w, s, zp
 
 

@@ -129,6 +129,18 @@ int qmoe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
                                                                                      : QMOE_ERR_CUDA;
 }
 
+int qmoe_workspace_set_diagnostics(void* workspace, size_t workspace_bytes, uint32_t wait_limit_kilocycles,
+                                   uint32_t flags, void* stream) {
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < kCtlBytes) return QMOE_ERR_WORKSPACE;
+  if (flags & ~(uint32_t)QMOE_DIAG_STALL_GEMM) return QMOE_ERR_INVALID_ARG;
+  static_assert(kCtlDiag == kCtlWaitLimit + 1, "diagnostic words are adjacent");
+  const uint32_t words[2] = {wait_limit_kilocycles, flags};
+  return cudaMemcpyAsync(static_cast<uint32_t*>(workspace) + kCtlWaitLimit, words, sizeof(words),
+                         cudaMemcpyHostToDevice, (cudaStream_t)stream) == cudaSuccess
+             ? QMOE_OK
+             : QMOE_ERR_CUDA;
+}
+
 int qmoe_route(const void* x, const void* router_w, int act_dtype, const float* router_bias, int T,
                int H, int E, int k, float* topk_w, int32_t* topk_ids, int32_t* expert_offsets,
                int32_t* perm, void* workspace, size_t workspace_bytes, void* stream) {
@@ -491,19 +503,19 @@ int qmoe_gptq_zero_offset(const int32_t* qzeros, size_t n_words, int32_t* offset
 
 int qmoe_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int E, int K, int N,
                      int block_size, int zero_offset, const int32_t* zero_offset_dev, uint8_t* w_out,
-                     void* scales_out, uint8_t* zp_out, void* stream) {
+                     void* scales_out, uint8_t* zp_out, uint32_t* status_dev, void* stream) {
   if (!qweight || !scales || !w_out || !scales_out || (qzeros == nullptr) != (zp_out == nullptr))
     return QMOE_ERR_INVALID_ARG;
   if (E < 1 || E > 65535 || N < 8 || N % 8 || K < 32 || K % 32 || !valid_bs(block_size) || K % block_size)
     return QMOE_ERR_INVALID_ARG;
   if (zero_offset != 0 && zero_offset != 1) return QMOE_ERR_INVALID_ARG;
   if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(w_out, 4) || !aligned(scales, 2) ||
-      !aligned(scales_out, 2) || !aligned(zero_offset_dev, 4))
+      !aligned(scales_out, 2) || !aligned(zero_offset_dev, 4) || !aligned(status_dev, 4))
     return QMOE_ERR_INVALID_ARG;
   int rc = check_device();
   if (rc) return rc;
   return cuda_status(launch_repack_gptq(qweight, qzeros, scales, E, K, N, block_size, zero_offset, zero_offset_dev,
-                                        w_out, scales_out, zp_out, (cudaStream_t)stream));
+                                        w_out, scales_out, zp_out, status_dev, (cudaStream_t)stream));
 }
 
 int qmoe_unpack_zero_points(const uint8_t* zp_packed, int rows, int nb, uint8_t* zp_out, void* stream) {

@@ -52,11 +52,15 @@ __global__ void __launch_bounds__(kTile * kRowsPerPass) transpose_kernel(const T
   }
 }
 
-// zp[e][n][g] = min(stored(g, n) + offset, 15) from qzeros[e][g][n / 8]:
-// a tile of 32 blocks x 32 words (256 columns) per CTA
+// zp[e][n][g] = stored(g, n) + offset from qzeros[e][g][n / 8]: a tile of
+// 32 blocks x 32 words (256 columns) per CTA.  A zero point above 15 (a
+// stored 15 with offset 1) is outside the 4-bit format: it is written as 15
+// and reported as QMOE_ST_RANGE in *status (when given), because the
+// weights of that block then differ from the checkpoint's.
 __global__ void __launch_bounds__(kTile * kRowsPerPass) gptq_zeros_kernel(const uint32_t* __restrict__ qz,
                                                                           uint8_t* __restrict__ zp, int nb, int N,
-                                                                          int offset, const int32_t* offset_dev) {
+                                                                          int offset, const int32_t* offset_dev,
+                                                                          uint32_t* status) {
   __shared__ uint32_t tile[kTile][kTile + 1];
   const int NW = N / 8;
   const uint32_t* src = qz + (size_t)blockIdx.z * nb * NW;
@@ -72,15 +76,18 @@ __global__ void __launch_bounds__(kTile * kRowsPerPass) gptq_zeros_kernel(const 
   __syncthreads();
   // thread (tx, ty): block g0 + tx, columns n0 + ty + 8 m
   const int g = g0 + tx;
+  bool over = false;
   for (int m = 0; m < kTile; ++m) {
     const int nl = ty + kRowsPerPass * m;  // 0 .. 255
     const int n = w0 * 8 + nl;
     if (g < nb && n < N) {
       const uint32_t word = tile[tx][nl >> 3];
       const int v = (int)((word >> (4 * (nl & 7))) & 15u) + off;
+      over |= v > 15;
       dst[(size_t)n * nb + g] = (uint8_t)(v > 15 ? 15 : v);
     }
   }
+  if (over && status) atomicOr(status, QMOE_ST_RANGE);
 }
 
 // offset_out = 1 if the lower median of all stored zero points is 7, else 0
@@ -142,7 +149,7 @@ static dim3 tgrid(int rows, int cols, int E) {
 
 cudaError_t launch_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int E, int K,
                                int N, int bs, int offset, const int32_t* offset_dev, uint8_t* w_out,
-                               void* scales_out, uint8_t* zp_out, cudaStream_t st) {
+                               void* scales_out, uint8_t* zp_out, uint32_t* status, cudaStream_t st) {
   const dim3 blk(kTile, kRowsPerPass);
   const int nb = K / bs;
   // weights: [E][K/8][N] words -> [E][N][K/8] words
@@ -153,7 +160,7 @@ cudaError_t launch_repack_gptq(const int32_t* qweight, const int32_t* qzeros, co
                                                                static_cast<uint16_t*>(scales_out), nb, N);
   if (qzeros)
     gptq_zeros_kernel<<<tgrid(nb, N / 8, E), blk, 0, st>>>(reinterpret_cast<const uint32_t*>(qzeros), zp_out, nb,
-                                                            N, offset, offset_dev);
+                                                            N, offset, offset_dev, status);
   return cudaGetLastError();
 }
 

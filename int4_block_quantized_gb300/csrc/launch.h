@@ -45,7 +45,7 @@ bool decode_fits(int mode, int T, int N, int K, int bs, bool has_zp, int k);
 // weight-format adapters (formats.cu)
 cudaError_t launch_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int E, int K,
                                int N, int bs, int offset, const int32_t* offset_dev, uint8_t* w_out,
-                               void* scales_out, uint8_t* zp_out, cudaStream_t st);
+                               void* scales_out, uint8_t* zp_out, uint32_t* status, cudaStream_t st);
 cudaError_t launch_gptq_zero_offset(const int32_t* qzeros, size_t n_words, int32_t* offset_out, cudaStream_t st);
 cudaError_t launch_unpack_zp(const uint8_t* in, uint8_t* out, int rows, int nb, cudaStream_t st);
 // fused decode layer (T <= kTokGroup): cudaErrorInvalidValue if the plan

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "qmoe.h"
+
 #ifdef __CUDACC__
 #define QMOE_HD __host__ __device__ __forceinline__
 #else
@@ -15,9 +17,7 @@
 namespace qmoe {
 
 // ---- device status word bits (workspace control block, word 0)
-constexpr uint32_t QMOE_ST_TIMEOUT = 1u;  // a bounded wait ran out
-constexpr uint32_t QMOE_ST_INDEX = 2u;    // an index check failed
-constexpr uint32_t QMOE_ST_RANGE = 4u;    // a value beyond a fixed-point accumulator's range
+// status bits: QMOE_ST_TIMEOUT, QMOE_ST_INDEX, QMOE_ST_RANGE (include/qmoe.h)
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 8;
@@ -26,6 +26,8 @@ constexpr int kMaxTopk = 8;
 constexpr int kCtlStatus = 0;         // u32 sticky status bits
 constexpr int kCtlGroupTicket = 1;    // u32 router: token tiles done with top-k
 constexpr int kCtlNtiles = 2;         // u32 prefill: number of token tiles
+constexpr int kCtlWaitLimit = 4;      // u32 grouped GEMM wait limit in units of 1024 SM cycles (0: ~2 s)
+constexpr int kCtlDiag = 5;           // u32 diagnostic flags (QMOE_DIAG_*)
 constexpr int kCtlSliceDone = 8;      // u32 x kMaxSplit, fused decode: clusters done with each output
                                       // slice (reset to 0 by the last arrival)
 // fused decode: int64 fixed-point (2^-32) output accumulator [T][H], zero

@@ -366,14 +366,17 @@ __host__ inline bool gemm_plan(int mode, bool as, int nb, bool has_zp, int& nst,
 // and the epilogue's wait for a finished accumulator) sleeps between polls,
 // so that the waiting warps leave the issue slots to the dequantisers and
 // the MMA issuer; the others poll with try_wait's own suspend hint.
+// `limit` (SM cycles) is the control block's kCtlWaitLimit x 1024 when that
+// is set, else kWaitLimitCycles: a test shortens it to drive every role's
+// give-up and drain path.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                              volatile int* abort, uint32_t nap_ns = 0) {
+                                              volatile int* abort, long long limit, uint32_t nap_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!(nap_ns ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u))) {
     if (nap_ns) __nanosleep(nap_ns);
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       set_status(status, QMOE_ST_TIMEOUT);
       *abort = 1;
       return false;
@@ -482,6 +485,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   pdl_wait();  // routing, token tiles and (down) the SwiGLU output come from earlier grids
   pdl_trigger();
   const int NT = (int)__ldcg(p.ctl + kCtlNtiles);
+  const uint32_t wlim_k = __ldcg(p.ctl + kCtlWaitLimit);
+  const uint32_t diag = __ldcg(p.ctl + kCtlDiag);
+  const long long wlim = wlim_k ? (long long)wlim_k << 10 : kWaitLimitCycles;
   const int ntile_total = NT * MB;
   const int4* tiles = reinterpret_cast<const int4*>(p.tiles);
 
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int nbox = (npad + kBoxRows - 1) / kBoxRows;
         const uint32_t btx = nbox * kBoxRows * 128 * (BLO ? 2 : 1);
         for (int kc = 0; kc < KC; ++kc, ++it, rs.next(nst)) {
-          if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort, kNapNs)) break;
+          if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort, wlim, kNapNs)) break;
           uint8_t* st = stages + rs.i * L.stage;
           uint64_t* fb = &b_full[rs.i];
           mbar_arrive_expect_tx(fb, btx);
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = blockIdx.x; t < ntile_total && !*s_abort; t += gridDim.x, ++tc, rz.next(nsz)) {
         const int4 tl = __ldcg(tiles + t % NT);
         const int mb = t / NT, e = tl.x;
-        if (tc >= nsz && !wait_or_abort(&sz_empty[rz.i], rz.ph ^ 1u, status, s_abort, kNapNs)) break;
+        if (tc >= nsz && !wait_or_abort(&sz_empty[rz.i], rz.ph ^ 1u, status, s_abort, wlim, kNapNs)) break;
         // block scales / zero points of the tile's 128 weight rows over the whole K
         uint8_t* sz = szbuf + rz.i * L.sz_bytes;
         uint64_t* zb = &sz_full[rz.i];
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (HAS_ZP) bulk_g2s(sz + sbytes, p.z[2] + r * nb, zbytes, zb);
         }
         for (int kc = 0; kc < KC; ++kc, ++ip, rp.next(npk)) {
-          if (ip >= npk && !wait_or_abort(&pk_empty[rp.i], rp.ph ^ 1u, status, s_abort, kNapNs)) break;
+          if (ip >= npk && !wait_or_abort(&pk_empty[rp.i], rp.ph ^ 1u, status, s_abort, wlim, kNapNs)) break;
           uint8_t* pk = pkbuf + rp.i * kPkBytes;
           uint64_t* fb = &pk_full[rp.i];
           mbar_arrive_expect_tx(fb, kPkBytes);
@@ -565,13 +571,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int4 tl = __ldcg(tiles + t % NT);
       const uint32_t idesc = idesc_f16(128, (tl.z + 15) & ~15, bf);
       const int b = tc & 1;
-      if (tc >= 2 && !wait_or_abort(&tmem_empty[b], ((tc >> 1) - 1) & 1, status, s_abort)) break;
+      if (tc >= 2 && !wait_or_abort(&tmem_empty[b], ((tc >> 1) - 1) & 1, status, s_abort, wlim)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + b * kBN;
       bool ok = true;
       for (int kc = 0; kc < KC; ++kc, rs.next(nst)) {
-        if (!wait_or_abort(&a_full[rs.i], rs.ph, status, s_abort, kMmaNapNs) ||
-            !wait_or_abort(&b_full[rs.i], rs.ph, status, s_abort, kMmaNapNs)) {
+        if (!wait_or_abort(&a_full[rs.i], rs.ph, status, s_abort, wlim, kMmaNapNs) ||
+            !wait_or_abort(&b_full[rs.i], rs.ph, status, s_abort, wlim, kMmaNapNs)) {
           ok = false;
           break;
         }
@@ -591,7 +597,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       mma_commit_elect(&tmem_full[b]);
     }
-    if (*s_abort && issued) {  // MMAs still in flight must finish before TMEM is freed
+    // every MMA must have finished before TMEM is freed: after an abort the
+    // epilogue may not have waited for the last accumulator
+    if (issued) {
       mma_commit_elect(fin);
       mbar_wait(fin, 0, nullptr);
     }
@@ -609,7 +617,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // latency overlaps the previous chunk's work.
     uint4 q = make_uint4(0, 0, 0, 0);
     if (nchunks > 0) {
-      if (wait_or_abort(&pk_full[0], 0, status, s_abort))
+      // QMOE_DIAG_STALL_GEMM: wait for the slot's second fill, which cannot
+      // come before this one is consumed, so the wait runs out (timeout test)
+      const uint32_t ph0 = (diag & QMOE_DIAG_STALL_GEMM) ? 1u : 0u;
+      if (wait_or_abort(&pk_full[0], ph0, status, s_abort, wlim))
         q = *reinterpret_cast<const uint4*>(pkbuf + r * 32 + hh * 16);
       else
         ok = false;
@@ -620,7 +631,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // keeps them for the next chunks: one conflicted load per 8 blocks.
     const bool vec = (nb & 7) == 0;
     for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x, rz.next(nsz)) {
-      if (!wait_or_abort(&sz_full[rz.i], rz.ph, status, s_abort)) break;
+      if (!wait_or_abort(&sz_full[rz.i], rz.ph, status, s_abort, wlim)) break;
       const uint8_t* sz = szbuf + rz.i * L.sz_bytes;
       const uint16_t* srow = reinterpret_cast<const uint16_t*>(sz) + (size_t)r * nb;
       const uint8_t* zrow = sz + 128u * nb * 2 + (size_t)r * nb;
@@ -664,10 +675,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (it + 1 < nchunks) {  // the next chunk's codes (the next ring slot)
           Ring rn = rp;
           rn.next(npk);
-          if (!wait_or_abort(&pk_full[rn.i], rn.ph, status, s_abort)) { ok = false; break; }
+          if (!wait_or_abort(&pk_full[rn.i], rn.ph, status, s_abort, wlim)) { ok = false; break; }
           q = *reinterpret_cast<const uint4*>(pkbuf + rn.i * kPkBytes + r * 32 + hh * 16);
         }
-        if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort)) { ok = false; break; }
+        if (it >= nst && !wait_or_abort(&empty[rs.i], rs.ph ^ 1u, status, s_abort, wlim)) { ok = false; break; }
         tc_fence_after();
         const uint32_t ta = a_row + rs.i * AW;
         tmem_st16(ta, h);
@@ -698,7 +709,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int mb = t / NT;
       const int row0 = tl.y, nrows = tl.z, npad = (nrows + 15) & ~15;
       const int b = tc & 1;
-      if (!wait_or_abort(&tmem_full[b], (tc >> 1) & 1, status, s_abort, kNapNs)) break;
+      if (!wait_or_abort(&tmem_full[b], (tc >> 1) & 1, status, s_abort, wlim, kNapNs)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
       for (int c0 = 0; c0 < npad; c0 += 16, ++cc) {
@@ -709,13 +720,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int xb = cc & 1;
           float* gx = gbuf + xb * kGbufFloats;
           if (q < 2) {
-            if (cc >= 2 && !wait_or_abort(&gx_empty[xb], ((cc >> 1) - 1) & 1, status, s_abort)) { ok = false; break; }
+            if (cc >= 2 && !wait_or_abort(&gx_empty[xb], ((cc >> 1) - 1) & 1, status, s_abort, wlim)) { ok = false; break; }
 #pragma unroll
             for (int j = 0; j < 16; ++j) gx[row * 17 + j] = __uint_as_float(v[j]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&gx_full[xb]);
           } else {
-            if (!wait_or_abort(&gx_full[xb], (cc >> 1) & 1, status, s_abort)) { ok = false; break; }
+            if (!wait_or_abort(&gx_full[xb], (cc >> 1) & 1, status, s_abort, wlim)) { ok = false; break; }
             const int i = row - 64;
             const int ig = mb * 64 + i;
             const size_t col = (ig & ~7) + kperm_pos(ig & 7);

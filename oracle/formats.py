@@ -71,8 +71,11 @@ def gptq_to_canonical(qweight, qzeros, scales, K, N, block_size, zero_offset):
     """One GPTQ matrix -> canonical (w [N, K/2] u8, scales [N, K/bs], zp [N, K/bs] u8 or None).
 
     `scales` is any 2-D array [K/bs, N] (16-bit patterns or floats); it is
-    transposed as stored.  Zero points above 15 after the offset saturate
-    at 15 (a stored 15 with offset 1 is outside the format)."""
+    transposed as stored.  A zero point above 15 after the offset (a stored
+    15 with offset 1) does not fit the canonical 4-bit zero point: it is
+    written as 15, which changes that block's weights by one scale step, and
+    gptq_zero_points_fit() reports it; the converter reports the same
+    condition as a device status bit."""
     nb = K // block_size
     qweight = np.asarray(qweight)
     w = np.zeros((N, K // 2), dtype=np.uint8)
@@ -90,6 +93,16 @@ def gptq_to_canonical(qweight, qzeros, scales, K, N, block_size, zero_offset):
             for g in range(nb):
                 zp[n, g] = min(gptq_stored_zero(qzeros, g, n) + zero_offset, 15)
     return w, s, zp
+
+
+def gptq_zero_points_fit(qzeros, K, N, block_size, zero_offset):
+    """True when every stored zero + offset is at most 15, i.e. the GPTQ
+    matrix converts to the canonical layout without changing a weight."""
+    if qzeros is None:
+        return True
+    qzeros = np.asarray(qzeros)
+    return all(gptq_stored_zero(qzeros, g, n) + zero_offset <= 15
+               for n in range(N) for g in range(K // block_size))
 
 
 def gptq_dequant(qweight, qzeros, scales, K, N, block_size, zero_offset):

@@ -145,7 +145,8 @@ def oracle_forward_parallel(L, nproc=None):
             present.append(n)
         ints = {n: int(L[n]) for n in _INTS}
         T = ints["T"]
-        nproc = max(1, min(T, nproc or os.cpu_count() or 1))
+        ncpu = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        nproc = max(1, min(T, nproc or ncpu))
         chunk = -(-T // nproc)
         jobs = [(folder, lo, min(T, lo + chunk), ints, present) for lo in range(0, T, chunk)]
         with mp.get_context("spawn").Pool(nproc) as pool:
@@ -155,3 +156,45 @@ def oracle_forward_parallel(L, nproc=None):
                 np.concatenate([p[3] for p in parts]), np.concatenate([p[4] for p in parts]))
     finally:
         shutil.rmtree(folder, ignore_errors=True)
+
+
+def tile_columns(ids, E, tile=128):
+    """Column of every assignment (token t, slot j) inside its expert's token
+    tile, for routing ids [T, k]: assignments are grouped by expert in
+    (token, slot) order, and an expert with n assignments is cut into
+    ceil(n / tile) tiles of ceil(n / tiles) rows.  Returns [T, k] ints."""
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    flat = ids.reshape(-1)
+    counts = np.bincount(flat, minlength=E)
+    rank = np.zeros(flat.size, dtype=np.int64)
+    seen = np.zeros(E, dtype=np.int64)
+    for a, e in enumerate(flat):
+        rank[a] = seen[e]
+        seen[e] += 1
+    ntile = (counts + tile - 1) // tile
+    rows = np.where(ntile > 0, (counts + np.maximum(ntile, 1) - 1) // np.maximum(ntile, 1), 1)
+    return (rank % rows[flat]).reshape(T, k)
+
+
+def tokens_covering_tile_columns(ids, E, n_extra, seed, tile=128):
+    """Token indices whose assignments together sit at every tile column
+    that occurs (greedy), plus n_extra more drawn at random."""
+    cols = tile_columns(ids, E, tile)
+    T = cols.shape[0]
+    need = set(int(c) for c in np.unique(cols))
+    chosen = []
+    for t in np.argsort([-len(set(r)) for r in cols.tolist()], kind="stable"):
+        new = set(int(c) for c in cols[t]) & need
+        if new:
+            chosen.append(int(t))
+            need -= new
+        if not need:
+            break
+    rest = np.setdiff1d(np.arange(T), chosen)
+    rng = np.random.default_rng(seed)
+    extra = rng.choice(rest, size=min(n_extra, rest.size), replace=False).tolist()
+    picked = sorted(set(chosen) | set(int(t) for t in extra))
+    covered = set(int(c) for c in np.unique(cols[picked]))
+    assert covered == set(int(c) for c in np.unique(cols)), "tile columns not all covered"
+    return picked

@@ -173,7 +173,7 @@ def test_adapters_reject_bad_arguments(L):
         return L.qmoe_repack_gptq(kw.get("qw", FAKE), kw.get("qz", FAKE), kw.get("s", FAKE), kw.get("E", 2),
                                   kw.get("K", 256), kw.get("N", 64), kw.get("bs", 32), kw.get("off", 1),
                                   kw.get("offdev", None), kw.get("w", FAKE), kw.get("so", FAKE),
-                                  kw.get("zp", FAKE), None)
+                                  kw.get("zp", FAKE), kw.get("st", None), None)
     assert repack(qw=None) == 1
     assert repack(w=None) == 1
     assert repack(qz=None) == 1              # zp_out given without qzeros
@@ -183,6 +183,7 @@ def test_adapters_reject_bad_arguments(L):
     assert repack(bs=16) == 1                # block size outside {32, 64, 128}
     assert repack(K=320, bs=128) == 1        # K not a multiple of the block size
     assert repack(off=2) == 1                # offset 0 or 1 only
+    assert repack(st=FAKE + 2) == 1          # status word not 4-byte aligned
     assert repack(E=0) == 1
     assert repack(qw=FAKE + 2) == 1          # int32 words must be 4-byte aligned
     assert repack(s=FAKE + 1) == 1           # scales must be 2-byte aligned

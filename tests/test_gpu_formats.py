@@ -87,6 +87,26 @@ def test_repack_gptq_full_layer_shape_sampled():
         assert (int(wc[e, n, k // 2]) >> (4 * (k % 2))) & 15 == F.gptq_nibble(_np_u32(qw[e]), k, n)
 
 
+def test_zero_point_16_is_reported():
+    """A stored zero of 15 with offset 1 is 16, outside the 4-bit zero point:
+    the converter writes 15 (like the oracle) and sets the range bit; the
+    binding's default check raises.  Offset 0 converts the same words
+    silently."""
+    E, K, N, bs = 1, 128, 16, 32
+    qw, qz, sc = _gptq(E, K, N, bs, seed=9, stored_zero=15)
+    with pytest.raises(B.QMoEError, match="above 15"):
+        B.qmoe_repack_gptq(qw.to(DEV), qz.to(DEV), sc.to(DEV), bs, zero_offset=1)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _, _, zp = B.qmoe_repack_gptq(qw.to(DEV), qz.to(DEV), sc.to(DEV), bs, zero_offset=1, check=False, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 4
+    assert not F.gptq_zero_points_fit(_np_u32(qz[0]), K, N, bs, 1)
+    _, _, rz = F.gptq_to_canonical(_np_u32(qw[0]), _np_u32(qz[0]), sc[0].view(torch.int16).numpy(), K, N, bs, 1)
+    assert np.array_equal(zp[0].cpu().numpy(), rz)
+    _, _, zp0 = B.qmoe_repack_gptq(qw.to(DEV), qz.to(DEV), sc.to(DEV), bs, zero_offset=0)
+    assert (zp0 == 15).all() and F.gptq_zero_points_fit(_np_u32(qz[0]), K, N, bs, 0)
+
+
 @pytest.mark.parametrize("stored,expect", [(7, 1), (8, 0)])
 def test_device_zero_offset_rule(stored, expect):
     _, qz, _ = _gptq(4, 256, 64, 32, seed=stored, stored_zero=stored)

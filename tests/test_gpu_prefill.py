@@ -14,7 +14,7 @@ import torch
 import oracle
 from int4_block_quantized_gb300 import binding as B
 from int4_block_quantized_gb300 import synthetic as S
-from qmoe_check import assert_close_layer, check_routing, oracle_forward_parallel
+from qmoe_check import assert_close_layer, check_routing, oracle_forward_parallel, tokens_covering_tile_columns
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -27,7 +27,10 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def check_prefill(wl, L=None, seed=0, sample=None, accumulate=False, path=B.PATH_PREFILL):
+def check_prefill(wl, L=None, seed=0, sample=None, accumulate=False, path=B.PATH_PREFILL, cover=None):
+    """cover = n: compare the tokens whose assignments sit at every column
+    position of the GEMM's token tiles (from the GPU's routing) plus n more
+    at random, instead of every token."""
     L = L or S.make_layer(wl, seed=seed, device=DEV)
     x = L["x"]
     T = x.shape[0]
@@ -41,7 +44,9 @@ def check_prefill(wl, L=None, seed=0, sample=None, accumulate=False, path=B.PATH
     torch.cuda.synchronize()
     rc, bits = ws.status()
     assert rc == 0 and bits == 0
-    if sample is None:
+    if cover is not None:
+        idx = np.asarray(tokens_covering_tile_columns(ti.cpu().numpy(), wl.E, cover, seed + 11))
+    elif sample is None:
         idx = np.arange(T)
     else:
         idx = np.sort(np.random.default_rng(seed + 11).choice(T, size=min(sample, T), replace=False))
@@ -90,17 +95,18 @@ def test_prefill_full_size_every_token():
 
 
 @pytest.mark.parametrize("name", ["e128_prefill", "e256_prefill"])
-def test_larger_e_prefill_full_size_every_token(name):
+def test_larger_e_prefill_full_size_tile_columns(name):
     """Larger-E family shapes: 128 experts / I = 768 and 256 experts / I = 512,
-    top-8, T = 512 through the grouped GEMM, every token."""
-    check_prefill(S.WORKLOADS[name], seed=4)
+    top-8, T = 512 through the grouped GEMM: tokens at every tile column
+    position that occurs, plus 128 more."""
+    check_prefill(S.WORKLOADS[name], seed=4, cover=128)
 
 
-def test_stack_layer_full_size_every_token():
+def test_stack_layer_full_size_tile_columns():
     """One layer of the T = 2048 stack shape (bf16 tokens, fp16 scales, zp):
-    all 2048 tokens, so every column position of every 128-token tile of
-    every expert is compared."""
-    check_prefill(S.WORKLOADS["stack"], seed=2)
+    the tokens whose assignments sit at every column position of the 128-
+    token tiles (all positions that occur), plus 256 more at random."""
+    check_prefill(S.WORKLOADS["stack"], seed=2, cover=256)
 
 
 def test_prefill_residual_accumulate():
@@ -153,6 +159,31 @@ def test_withdrawn_path_value_is_rejected():
     L = S.make_layer(wl, seed=1, device=DEV)
     with pytest.raises(RuntimeError, match="invalid argument"):
         B.qmoe_forward(L, path=3)
+
+
+def test_gemm_wait_timeout_is_reported_and_the_workspace_recovers():
+    """Drive the grouped GEMM's bounded waits to expiry: the dequantisers
+    wait for a copy that cannot arrive (a flag nothing sets) under a wait
+    limit of 2^20 SM cycles (about 0.5 ms).  The wait gives up, every role
+    drains what it has in flight, TMEM is freed and both GEMM kernels
+    return; the status reads QMOE_ERR_TIMEOUT.  With the diagnostics cleared
+    the same workspace computes the same output bit for bit."""
+    wl = S.Workload("pf_timeout", 40, 256, 128, 8, 2, 32, S.F16, S.F16, True, -5)
+    L = S.make_layer(wl, seed=3, device=DEV)
+    ws = B.Workspace(wl.T, wl.H, wl.I, wl.E, wl.k)
+    ref = B.qmoe_forward(L, ws=ws, path=B.PATH_PREFILL).clone()
+    torch.cuda.synchronize()
+    assert ws.status() == (0, 0)
+    ws.set_diagnostics(1024, B.DIAG_STALL_GEMM)
+    B.qmoe_forward(L, ws=ws, path=B.PATH_PREFILL)
+    torch.cuda.synchronize()
+    rc, bits = ws.status()
+    assert rc == 5 and (bits & 1), (rc, bits)
+    ws.set_diagnostics(0, 0)
+    out = B.qmoe_forward(L, ws=ws, path=B.PATH_PREFILL)
+    torch.cuda.synchronize()
+    assert ws.status() == (0, 0)
+    assert torch.equal(out, ref)
 
 
 def test_bf16_beyond_fp16_range_sets_the_range_bit():

@@ -44,8 +44,12 @@ def test_gptq_zero_points_match_hand_values():
     _, _, z0 = F.gptq_to_canonical(QWEIGHT_HAND, QZEROS_HAND, scales, 32, 8, 32, 0)
     _, _, z1 = F.gptq_to_canonical(QWEIGHT_HAND, QZEROS_HAND, scales, 32, 8, 32, 1)
     assert z0[:, 0].tolist() == [7, 7, 3, 0, 15, 8, 1, 2]
-    # offset 1; the stored 15 would be 16, outside 4 bits: saturates at 15
+    # offset 1; the stored 15 would be 16, outside 4 bits: written as 15 and
+    # reported as not fitting
     assert z1[:, 0].tolist() == [8, 8, 4, 1, 15, 9, 2, 3]
+    assert F.gptq_zero_points_fit(QZEROS_HAND, 32, 8, 32, 0)
+    assert not F.gptq_zero_points_fit(QZEROS_HAND, 32, 8, 32, 1)
+    assert F.gptq_zero_points_fit(None, 32, 8, 32, 1)
 
 
 def test_zero_offset_rule_of_the_pages():
