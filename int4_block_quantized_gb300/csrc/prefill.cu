@@ -617,13 +617,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // latency overlaps the previous chunk's work.
     uint4 q = make_uint4(0, 0, 0, 0);
     if (nchunks > 0) {
-      // QMOE_DIAG_STALL_GEMM: wait for the slot's second fill, which cannot
-      // come before this one is consumed, so the wait runs out (timeout test)
-      const uint32_t ph0 = (diag & QMOE_DIAG_STALL_GEMM) ? 1u : 0u;
-      if (wait_or_abort(&pk_full[0], ph0, status, s_abort, wlim))
-        q = *reinterpret_cast<const uint4*>(pkbuf + r * 32 + hh * 16);
-      else
-        ok = false;
+      ok = wait_or_abort(&pk_full[0], 0, status, s_abort, wlim);
+      // QMOE_DIAG_STALL_GEMM: then wait for the slot's second fill (phase
+      // 1), which cannot come before this one is consumed, so the wait runs
+      // out (timeout test).  A wait on parity 1 before phase 0 has completed
+      // would return at once: it asks for the phase before the first.
+      if (ok && (diag & QMOE_DIAG_STALL_GEMM)) ok = wait_or_abort(&pk_full[0], 1, status, s_abort, wlim);
+      if (ok) q = *reinterpret_cast<const uint4*>(pkbuf + r * 32 + hh * 16);
     }
     // The rows of a tile's scales sit nb * 2 bytes apart: at 128 bytes the 32
     // rows of a warp fall into one bank.  When rows are 16-byte aligned a

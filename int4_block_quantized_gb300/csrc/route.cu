@@ -20,8 +20,11 @@
 // last CTA to finish.  Deterministic: no floating-point atomics.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 
 namespace qmoe {
 
@@ -383,6 +386,226 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   }
 }
 
+// ------------------------------------------------------------ many tokens
+// Tensor-core router for T > 16: one cluster of kMaxSplit CTAs per tile of
+// 128 tokens.  CTA s reduces its share of H in 64-wide K chunks with
+// tcgen05.mma (M = 128 tokens, N = E rounded up to 16, fp32 accumulation in
+// TMEM): the x tile arrives by TMA (128-byte swizzle, rows past T read as
+// zero) and the CTA's threads transpose the router rows into the K-major
+// operand.  The router weight is read once per 128 tokens instead of once
+// per 8.  Products of two 16-bit values are exact in fp32; the sums are
+// fp32 (tensor-core accumulation order).  The kMaxSplit partial-logit tiles
+// are summed in rank order through distributed shared memory, then softmax
+// + top-k per token and the grouping, as in the small-T kernel.
+constexpr int kRtTok = 128;
+QMOE_HD int rt_np(int E) { return (E + 15) & ~15; }
+QMOE_HD uint32_t rt_stage_bytes(int E) { return 16384u + (uint32_t)rt_np(E) * 128u; }
+QMOE_HD size_t rt_smem_bytes(int T, int E, int k) {
+  // [barriers][2 stages: x tile 16 KB + router operand NP x 128 B][partials 128 x (NP + 1) fp32]
+  const size_t compute = 1024 + 2 * (size_t)rt_stage_bytes(E) + (size_t)kRtTok * (rt_np(E) + 1) * 4 + 1024;
+  const size_t A = (size_t)T * k;
+  const size_t group = A > 256 ? 4 * route_group_ints((int)A, E) + 2048 : 0;  // after the 1 KB header, + alignment
+  return compute > group ? compute : group;
+}
+
+template <typename TA, int ME>
+__global__ void __launch_bounds__(kRouteThreads) route_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                                 RouteParams p) {
+  extern __shared__ __align__(1024) uint8_t rsm_raw[];
+  uint8_t* sm = rsm_raw + ((1024u - (smem_u32(rsm_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm);  // [2] x tile landed
+  uint64_t* mmad = full + 2;                         // [2] MMAs done with the stage
+  uint64_t* acc_done = full + 4;                     // all MMAs done
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 5);
+  __shared__ int sh_last;
+  const int E = p.E, H = p.H, k = p.k, NP = rt_np(E), PS = NP + 1;
+  const uint32_t SB = rt_stage_bytes(E);
+  uint8_t* stages = sm + 1024;
+  float* part = reinterpret_cast<float*>(stages + 2 * SB);  // [128][PS]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t* status = p.ctl + kCtlStatus;
+  const uint32_t rank = cluster_ctarank();
+  const int t0 = blockIdx.y * kRtTok;
+  const int nkc = H / 64, cpr = (nkc + kMaxSplit - 1) / kMaxSplit;
+  const int c0 = (int)rank * cpr, nc = max(0, min(nkc, c0 + cpr) - c0);
+  const uint32_t tcols = NP > 64 ? 128u : NP > 32 ? 64u : 32u;
+  const uint16_t* rw = static_cast<const uint16_t*>(p.router_w);
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *s_tmem;
+  pdl_wait();  // x may be the previous kernel's output
+  pdl_trigger();
+  bool ok = true;
+  const uint32_t idesc = idesc_f16(128, NP, std::is_same<TA, __nv_bfloat16>::value);
+  for (int c = 0; c < nc; ++c) {
+    const int s = c & 1;
+    uint8_t* st = stages + s * SB;
+    if (c >= 2) ok = mbar_wait(&mmad[s], ((c - 2) >> 1) & 1, status) && ok;  // stage free
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&full[s], 16384u);
+      tma_load_2d(st, &tm_x, (c0 + c) * 64, t0, &full[s]);
+    }
+    // router rows k0 .. k0 + 63 as the K-major operand [NP][64]: 16-byte
+    // group g of row n at (n / 8) * 1024 + (n % 8) * 128 + (g ^ (n % 8)) * 16
+    const int k0 = (c0 + c) * 64;
+    for (int idx = tid; idx < 8 * NP; idx += kRouteThreads) {
+      const int n = idx % NP, g = idx / NP;
+      uint32_t w4[4] = {0u, 0u, 0u, 0u};
+      if (n < E) {
+        const uint16_t* src = rw + (size_t)(k0 + 8 * g) * E + n;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          w4[i] = (uint32_t)__ldg(src + (size_t)(2 * i) * E) | ((uint32_t)__ldg(src + (size_t)(2 * i + 1) * E) << 16);
+      }
+      *reinterpret_cast<uint4*>(st + 16384 + (n >> 3) * 1024 + (n & 7) * 128 + ((g ^ (n & 7)) << 4)) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads these through the async proxy
+    __syncthreads();
+    if (warp == 0) {
+      ok = mbar_wait(&full[s], (c >> 1) & 1, status) && ok;
+      tc_fence_after();
+      if (ok) {
+        const uint64_t ad = sw128_desc(smem_u32(st)), bd = sw128_desc(smem_u32(st + 16384));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_f16_ss_elect(tb, ad + 2 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
+      }
+      mma_commit_elect(&mmad[s]);
+    }
+  }
+  if (warp == 0) mma_commit_elect(acc_done);
+  ok = mbar_wait(acc_done, 0, status) && ok;
+  tc_fence_after();
+  // partial logits of this CTA's share of H: warp w < 4 reads TMEM lanes
+  // (tokens) 32w .. 32w + 31
+  if (warp < 4) {
+    const int tl = warp * 32 + lane;
+    for (int c16 = 0; c16 < NP; c16 += 16) {
+      uint32_t v[16];
+      if (nc > 0 && ok) {
+        tmem_ld16(tb + ((uint32_t)(warp * 32) << 16) + (uint32_t)c16, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) part[tl * PS + c16 + j] = __uint_as_float(v[j]);
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // every CTA's partials are complete
+  // ---- this CTA's 16 tokens: rank-ordered sum of the partials, softmax, top-k
+  for (int q = 0; q < kRtTok / kMaxSplit / (kRouteThreads / 32); ++q) {
+    const int tl = (int)rank * (kRtTok / kMaxSplit) + q * (kRouteThreads / 32) + warp;
+    const int t = t0 + tl;
+    if (t < p.T) {
+      float lg[ME];
+#pragma unroll
+      for (int m = 0; m < ME; ++m) {
+        const int e = lane + 32 * m;
+        if (e < E) {
+          float v = 0.f;
+#pragma unroll
+          for (int r = 0; r < kMaxSplit; ++r) v += ld_dsmem_f32(part + tl * PS + e, (uint32_t)r);
+          lg[m] = v + (p.bias ? p.bias[e] : 0.f);
+        } else {
+          lg[m] = -INFINITY;
+        }
+      }
+      int ids[kMaxTopk];
+      float wts[kMaxTopk];
+      softmax_topk<ME>(lg, E, k, p.gate_sigmoid != 0, lane, ids, wts);
+      if (lane < k) {
+        int bi = 0;
+        float bp = 0.f;
+#pragma unroll
+        for (int qq = 0; qq < kMaxTopk; ++qq)
+          if (qq == lane) {
+            bi = ids[qq];
+            bp = wts[qq];
+          }
+        const size_t a = (size_t)t * k + lane;
+        p.topk_ids[a] = bi;
+        p.topk_w[a] = bp;
+        if (p.user_ids) p.user_ids[a] = bi;
+        if (p.user_w) p.user_w[a] = bp;
+      }
+    }
+  }
+  cluster_sync_all();  // peers keep their partials until the reads above are done
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, tcols);
+  }
+  const int A = p.T * k;
+  int* smem_i = reinterpret_cast<int*>(sm + 1024);
+  // ---- the last CTA to finish groups all assignments by expert
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t ticket = atomicAdd(p.ctl + kCtlGroupTicket, 1u);
+    sh_last = (ticket == gridDim.x * gridDim.y - 1);
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  if (tid == 0) p.ctl[kCtlGroupTicket] = 0u;
+  if (A <= 256) {
+    if (warp == 0) group_one_warp(p.topk_ids, true, A, E, smem_i, smem_i + E, p, lane, status);
+  } else {
+    group_chunked(A, E, smem_i, p, tid, status);
+  }
+}
+
+bool route_tc_fits(int T, int H, int E, int k) {
+  return T > kDecodeMaxTokens && H % 64 == 0 && H >= 64 && E >= 1 && E <= 128 &&
+         rt_smem_bytes(T, E, k) <= 227 * 1024;
+}
+
+template <typename TA, int ME>
+static cudaError_t launch_route_tc_me(const RouteParams& p, int act_dtype, cudaStream_t st, bool pdl) {
+  CUtensorMap m;
+  if (!make_map(&m, p.x, act_dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                (uint64_t)p.H, (uint64_t)p.T, 64, kRtTok, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorNotSupported;
+  const size_t smem = rt_smem_bytes(p.T, p.E, p.k);
+  auto fn = route_tc_kernel<TA, ME>;
+  cudaError_t err = ensure_smem(fn, smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kMaxSplit, (p.T + kRtTok - 1) / kRtTok);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kMaxSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, fn, m, p);
+}
+
+template <typename TA>
+static cudaError_t launch_route_tc(const RouteParams& p, int act_dtype, cudaStream_t st, bool pdl) {
+  const int me = (p.E + 31) / 32;
+  if (me <= 1) return launch_route_tc_me<TA, 1>(p, act_dtype, st, pdl);
+  if (me <= 2) return launch_route_tc_me<TA, 2>(p, act_dtype, st, pdl);
+  return launch_route_tc_me<TA, 4>(p, act_dtype, st, pdl);
+}
+
 template <typename TA, int ME, int TOK>
 static cudaError_t launch_route_me(const RouteParams& p, cudaStream_t st, bool pdl, size_t smem) {
   const int tiles = (p.T + TOK - 1) / TOK;
@@ -421,6 +644,9 @@ static cudaError_t launch_route_t(const RouteParams& p, cudaStream_t st, bool pd
 }
 
 cudaError_t launch_route(const RouteParams& p, int act_dtype, cudaStream_t st, bool pdl) {
+  if (route_tc_fits(p.T, p.H, p.E, p.k) && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0)
+    return act_dtype == 1 ? launch_route_tc<__nv_bfloat16>(p, act_dtype, st, pdl)
+                          : launch_route_tc<__half>(p, act_dtype, st, pdl);
   return act_dtype == 1 ? launch_route_t<__nv_bfloat16>(p, st, pdl)
                         : launch_route_t<__half>(p, st, pdl);
 }

@@ -82,6 +82,11 @@ ROUTE_CASES = [
     ("e256", 5, 256, 256, 8, S.F16, 0.0),
     ("e1", 3, 64, 1, 1, S.F16, 0.0),
     ("stack", 2048, 2048, 60, 4, S.BF16, 0.0),
+    # T > 16 takes the tensor-core router: ragged last tile, E not a
+    # multiple of 16, H whose 64-wide chunks do not divide over 8 CTAs
+    ("tc_tail", 300, 256, 16, 2, S.F16, 0.0),
+    ("tc_e100", 129, 1024, 100, 6, S.BF16, 0.0),
+    ("tc_h192", 64, 192, 24, 3, S.F16, 0.0),
 ]
 
 
@@ -111,6 +116,19 @@ def test_route_ties_lower_id_first():
     x = torch.randn((T, H), generator=g, device=DEV).half()
     col = torch.randn((H, 1), generator=g, device=DEV) * 0.1
     rw = col.repeat(1, E).half()  # all logits equal
+    tw, ti, off, perm = B.qmoe_route(x, rw, k)
+    assert ti.cpu().tolist() == [[0, 1, 2, 3]] * T
+    assert torch.allclose(tw.cpu(), torch.full((T, k), 1.0 / E))
+
+
+def test_route_ties_lower_id_first_many_tokens():
+    """The same on the tensor-core router (T > 16): identical columns give
+    bit-identical logits, and the lower expert id wins."""
+    T, H, E, k = 40, 256, 16, 4
+    g = _gen(8)
+    x = torch.randn((T, H), generator=g, device=DEV).half()
+    col = torch.randn((H, 1), generator=g, device=DEV) * 0.1
+    rw = col.repeat(1, E).half()
     tw, ti, off, perm = B.qmoe_route(x, rw, k)
     assert ti.cpu().tolist() == [[0, 1, 2, 3]] * T
     assert torch.allclose(tw.cpu(), torch.full((T, k), 1.0 / E))
