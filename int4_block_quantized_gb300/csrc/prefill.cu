@@ -11,7 +11,7 @@
 // weighted sum from IR guide 3, Expert Computation steps 5-7.
 //
 // GB300 design.  Swap-AB: the weight rows are the MMA's M = 128 operand and
-// an expert's tokens (up to 128 per tile) its N, so small experts still fill
+// an expert's tokens (up to 192 per tile) its N, so small experts still fill
 // the tensor core's M dimension.  A gate-up tile stacks 64 gate rows over
 // the same 64 up rows, so gate and up land in one TMEM accumulator and the
 // SwiGLU pairs them in the epilogue.  Per CTA (one per SM, persistent):
@@ -43,7 +43,12 @@
 namespace qmoe {
 
 constexpr int kGemmThreads = 512;  // 16 warps (roles listed at the kernel)
-constexpr int kBN = 128;           // max tokens per tile (TMEM columns per accumulator)
+constexpr int kBN = 192;           // max tokens per tile (TMEM columns per accumulator)
+// Token tiles of an expert with n assignments: one tile when n <= kBN (its
+// weights dequantised once, wide MMAs), else ceil(n / 128) tiles of
+// balanced size: splitting a large expert finer keeps the per-CTA work of
+// the persistent schedule even.
+__host__ __device__ inline int token_tiles(int n) { return n <= kBN ? (n > 0 ? 1 : 0) : (n + 127) / 128; }
 constexpr int kBoxRows = 32;       // token rows per B TMA box
 constexpr int kModeGU = 0, kModeDN = 1;
 
@@ -79,7 +84,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint16_t* __restrict
     int n = 0, tl = 0;
     if (e < p.E) {
       n = __ldcg(p.offsets + e + 1) - __ldcg(p.offsets + e);
-      tl = (n + kBN - 1) / kBN;
+      tl = token_tiles(n);
     }
     s_scan[e] = tl;
     __syncthreads();
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(256) dense_setup_kernel(const uint16_t* __rest
       perm[r] = r;
       w[r] = 1.f;
     }
-    const int nt = (M + kBN - 1) / kBN, rows = (M + nt - 1) / nt;
+    const int nt = token_tiles(M), rows = (M + nt - 1) / nt;
     for (int i = threadIdx.x; i < nt; i += blockDim.x) {
       int32_t* d = p.tiles + 4 * i;
       d[0] = 0;
@@ -297,13 +302,13 @@ __device__ __forceinline__ void split_act(float a, uint16_t& h, uint16_t& l) {
 }
 
 // ------------------------------------------------------------ grouped GEMM
-constexpr uint32_t kTileOp = 128 * 128;    // 16-bit token tile: 128 rows x 64 K (SW128)
+constexpr uint32_t kTileOp = kBN * 128;    // 16-bit token tile: up to kBN rows x 64 K (SW128)
 constexpr uint32_t kPkBytes = 128 * 32;    // packed codes: 128 rows x 64 codes
 constexpr int kMaxPk = 24;                 // packed-code ring slots (at most)
-constexpr int kMaxSt = 4;                  // operand stages (at most)
+constexpr int kMaxSt = 4;                  // operand stages (at most; 2 with hi + lo weights)
 constexpr uint32_t kGbufFloats = 64 * 17;  // gate values of one 16-column chunk (padded rows)
 constexpr uint32_t kTmemCols = 512;        // the whole TMEM of the SM (one CTA per SM)
-constexpr uint32_t kAccCols = 2 * kBN;     // two 128-column accumulators, then the weight stages
+constexpr uint32_t kAccCols = 2 * kBN;     // two 192-column accumulators, then the weight stages
 constexpr uint32_t kSmemLimit = 232448;    // 227 KB per CTA
 constexpr uint32_t kNapNs = 256;          // poll interval of the off-critical-path waits
 constexpr uint32_t kMmaNapNs = 32;        // poll interval of the MMA issuer's waits (see the issuer)
@@ -317,9 +322,11 @@ constexpr int kDeqWarps = 8;               // two per sub-partition: row = warp%
 //   10     weight producer: packed codes (deep ring) and each tile's scales / zero points
 //   11     idle
 //   12-15  epilogue (TMEM lane quadrant = warp % 4)
-// TMEM columns: [0, 256) the two accumulators; from 256 one weight operand
+// TMEM columns: [0, 384) the two accumulators (token tiles of up to 192
+// columns: an expert with up to 192 assignments is one tile, so its weights
+// are dequantised once and each MMA is wide); from 384 one weight operand
 // stage per 64-wide K chunk: 32 columns (64 16-bit values per row), twice
-// that with hi + lo.
+// that with hi + lo, so 4 stages or 2.
 // Shared memory: [barriers][scale buffers][token stages: B hi, B lo][packed ring][exchange]
 struct GemmSmem {
   uint32_t b_lo, stage;  // offset of the low tile inside a token stage, stage size
@@ -340,14 +347,17 @@ __host__ __device__ inline GemmSmem gemm_smem(int mode, bool as, int nb, bool ha
 }
 // Pipeline plan.  Two tile-scale buffers first (with one, the weight
 // producer cannot start the next tile's codes until the current tile is
-// dequantised), then 4 operand stages down to 2 while at least 12 packed
-// slots remain; the packed ring takes the rest (<= 24 slots).  Long
-// reductions with small blocks (large whole-K scale buffers) fall back to
-// one scale buffer and as few as 4 packed slots.  Four stages fit TMEM with
-// hi + lo weights (4 x 64 columns after the accumulators).
-__host__ inline bool gemm_plan(int mode, bool as, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
+// dequantised), then as many operand stages as TMEM holds (4, or 2 with hi
+// + lo weights) down to 2 while at least 12 packed slots remain; the packed
+// ring takes the rest (<= 24 slots).  Long reductions with small blocks
+// (large whole-K scale buffers) fall back to one scale buffer and as few as
+// 4 packed slots.
+__host__ __device__ constexpr int gemm_max_stages(bool ws) {
+  return (int)((512u - kAccCols) / (ws ? 64u : 32u)) < kMaxSt ? (int)((512u - kAccCols) / (ws ? 64u : 32u)) : kMaxSt;
+}
+__host__ inline bool gemm_plan(int mode, bool ws, bool as, int nb, bool has_zp, int& nst, int& nsz, int& npk) {
   for (int sz = 2; sz >= 1; --sz)
-    for (int st = kMaxSt; st >= 2; --st) {
+    for (int st = gemm_max_stages(ws); st >= 2; --st) {
       const int pmin = sz == 1 && st == 2 ? 4 : 12;
       int pk = kMaxPk;
       while (pk >= pmin && gemm_smem(mode, as, nb, has_zp, st, sz, pk).total > kSmemLimit) --pk;
@@ -797,18 +807,15 @@ static inline GemmOps gemm_ops(int act_dtype, int scale_dtype, bool has_zp) {
 
 bool dense_fits(int N, int K, int bs, int act_dtype, int scale_dtype, bool has_zp) {
   if (N % 128 || K % 64 || bs < 32 || (bs & (bs - 1))) return false;
-  (void)act_dtype;
-  (void)scale_dtype;
   int a, b, c;
-  return gemm_plan(kModeDN, false, K / bs, has_zp, a, b, c);
+  return gemm_plan(kModeDN, gemm_ops(act_dtype, scale_dtype, has_zp).ws, false, K / bs, has_zp, a, b, c);
 }
 
 bool prefill_fits(int H, int I, int bs, int act_dtype, int scale_dtype, bool has_zp_gu, bool has_zp_d) {
   if (H % 128 || I % 64 || bs < 32 || (bs & (bs - 1))) return false;
-  (void)act_dtype;
-  (void)scale_dtype;
   int a, b, c;
-  return gemm_plan(kModeGU, false, H / bs, has_zp_gu, a, b, c) && gemm_plan(kModeDN, true, I / bs, has_zp_d, a, b, c);
+  return gemm_plan(kModeGU, gemm_ops(act_dtype, scale_dtype, has_zp_gu).ws, false, H / bs, has_zp_gu, a, b, c) &&
+         gemm_plan(kModeDN, gemm_ops(act_dtype, scale_dtype, has_zp_d).ws, true, I / bs, has_zp_d, a, b, c);
 }
 
 bool prefill_x_to_f16(int act_dtype, int scale_dtype) { return scale_dtype == 1 && act_dtype == 1; }
@@ -823,7 +830,7 @@ template <int MODE, typename OT, typename TS, bool Z, bool WS, bool AS>
 static cudaError_t launch_gemm_t(PrefillParams p, const CUtensorMap* m, cudaStream_t st, bool pdl) {
   const int K = (MODE == kModeGU) ? p.H : p.I;
   constexpr bool BLO = AS && MODE == kModeDN;
-  if (!gemm_plan(MODE, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk)) return cudaErrorInvalidValue;
+  if (!gemm_plan(MODE, WS, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk)) return cudaErrorInvalidValue;
   const GemmSmem L = gemm_smem(MODE, BLO, K / p.bs, Z, p.nst, p.nsz, p.npk);
   // the kernel takes all of the SM's TMEM: at least half the shared memory
   // keeps a second CTA off the SM

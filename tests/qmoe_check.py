@@ -158,11 +158,12 @@ def oracle_forward_parallel(L, nproc=None):
         shutil.rmtree(folder, ignore_errors=True)
 
 
-def tile_columns(ids, E, tile=128):
+def tile_columns(ids, E, tile=192):
     """Column of every assignment (token t, slot j) inside its expert's token
     tile, for routing ids [T, k]: assignments are grouped by expert in
-    (token, slot) order, and an expert with n assignments is cut into
-    ceil(n / tile) tiles of ceil(n / tiles) rows.  Returns [T, k] ints."""
+    (token, slot) order, and an expert with n assignments is one tile when
+    n <= tile, else ceil(n / 128) tiles of ceil(n / tiles) rows.  Returns
+    [T, k] ints."""
     ids = np.asarray(ids)
     T, k = ids.shape
     flat = ids.reshape(-1)
@@ -172,12 +173,13 @@ def tile_columns(ids, E, tile=128):
     for a, e in enumerate(flat):
         rank[a] = seen[e]
         seen[e] += 1
-    ntile = (counts + tile - 1) // tile
+    # one tile when n <= tile, else ceil(n / 128) tiles of balanced size
+    ntile = np.where(counts <= tile, (counts > 0).astype(np.int64), (counts + 127) // 128)
     rows = np.where(ntile > 0, (counts + np.maximum(ntile, 1) - 1) // np.maximum(ntile, 1), 1)
     return (rank % rows[flat]).reshape(T, k)
 
 
-def tokens_covering_tile_columns(ids, E, n_extra, seed, tile=128):
+def tokens_covering_tile_columns(ids, E, n_extra, seed, tile=192):
     """Token indices whose assignments together sit at every tile column
     that occurs (greedy), plus n_extra more drawn at random."""
     cols = tile_columns(ids, E, tile)
