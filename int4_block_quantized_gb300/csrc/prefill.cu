@@ -11,7 +11,7 @@
 // weighted sum from IR guide 3, Expert Computation steps 5-7.
 //
 // GB300 design.  Swap-AB: the weight rows are the MMA's M = 128 operand and
-// an expert's tokens (up to 192 per tile) its N, so small experts still fill
+// an expert's tokens (up to 160 per tile) its N, so small experts still fill
 // the tensor core's M dimension.  A gate-up tile stacks 64 gate rows over
 // the same 64 up rows, so gate and up land in one TMEM accumulator and the
 // SwiGLU pairs them in the epilogue.  Per CTA (one per SM, persistent):
@@ -43,7 +43,7 @@
 namespace qmoe {
 
 constexpr int kGemmThreads = 512;  // 16 warps (roles listed at the kernel)
-constexpr int kBN = 192;           // max tokens per tile (TMEM columns per accumulator)
+constexpr int kBN = 160;           // max tokens per tile (TMEM columns per accumulator)
 // Token tiles of an expert with n assignments: one tile when n <= kBN (its
 // weights dequantised once, wide MMAs), else ceil(n / 128) tiles of
 // balanced size: splitting a large expert finer keeps the per-CTA work of
@@ -305,10 +305,10 @@ __device__ __forceinline__ void split_act(float a, uint16_t& h, uint16_t& l) {
 constexpr uint32_t kTileOp = kBN * 128;    // 16-bit token tile: up to kBN rows x 64 K (SW128)
 constexpr uint32_t kPkBytes = 128 * 32;    // packed codes: 128 rows x 64 codes
 constexpr int kMaxPk = 24;                 // packed-code ring slots (at most)
-constexpr int kMaxSt = 4;                  // operand stages (at most; 2 with hi + lo weights)
+constexpr int kMaxSt = 4;                  // operand stages (at most; 3 with hi + lo weights)
 constexpr uint32_t kGbufFloats = 64 * 17;  // gate values of one 16-column chunk (padded rows)
 constexpr uint32_t kTmemCols = 512;        // the whole TMEM of the SM (one CTA per SM)
-constexpr uint32_t kAccCols = 2 * kBN;     // two 192-column accumulators, then the weight stages
+constexpr uint32_t kAccCols = 2 * kBN;     // two 160-column accumulators, then the weight stages
 constexpr uint32_t kSmemLimit = 232448;    // 227 KB per CTA
 constexpr uint32_t kNapNs = 256;          // poll interval of the off-critical-path waits
 constexpr uint32_t kMmaNapNs = 32;        // poll interval of the MMA issuer's waits (see the issuer)
@@ -322,11 +322,13 @@ constexpr int kDeqWarps = 8;               // two per sub-partition: row = warp%
 //   10     weight producer: packed codes (deep ring) and each tile's scales / zero points
 //   11     idle
 //   12-15  epilogue (TMEM lane quadrant = warp % 4)
-// TMEM columns: [0, 384) the two accumulators (token tiles of up to 192
-// columns: an expert with up to 192 assignments is one tile, so its weights
-// are dequantised once and each MMA is wide); from 384 one weight operand
+// TMEM columns: [0, 320) the two accumulators (token tiles of up to 160
+// columns: an expert with up to 160 assignments is one tile, so its weights
+// are dequantised once and each MMA is wide); from 320 one weight operand
 // stage per 64-wide K chunk: 32 columns (64 16-bit values per row), twice
-// that with hi + lo, so 4 stages or 2.
+// that with hi + lo, so 4 stages, or 3 with hi + lo.  (Measured: 160-column
+// tiles with 3 hi + lo stages beat 192 with 2 and 128 with 4 on the
+// 2048-token stack layer.)
 // Shared memory: [barriers][scale buffers][token stages: B hi, B lo][packed ring][exchange]
 struct GemmSmem {
   uint32_t b_lo, stage;  // offset of the low tile inside a token stage, stage size
@@ -347,7 +349,7 @@ __host__ __device__ inline GemmSmem gemm_smem(int mode, bool as, int nb, bool ha
 }
 // Pipeline plan.  Two tile-scale buffers first (with one, the weight
 // producer cannot start the next tile's codes until the current tile is
-// dequantised), then as many operand stages as TMEM holds (4, or 2 with hi
+// dequantised), then as many operand stages as TMEM holds (4, or 3 with hi
 // + lo weights) down to 2 while at least 12 packed slots remain; the packed
 // ring takes the rest (<= 24 slots).  Long reductions with small blocks
 // (large whole-K scale buffers) fall back to one scale buffer and as few as

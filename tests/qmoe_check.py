@@ -158,7 +158,7 @@ def oracle_forward_parallel(L, nproc=None):
         shutil.rmtree(folder, ignore_errors=True)
 
 
-def tile_columns(ids, E, tile=192):
+def tile_columns(ids, E, tile=160):
     """Column of every assignment (token t, slot j) inside its expert's token
     tile, for routing ids [T, k]: assignments are grouped by expert in
     (token, slot) order, and an expert with n assignments is one tile when
@@ -179,7 +179,7 @@ def tile_columns(ids, E, tile=192):
     return (rank % rows[flat]).reshape(T, k)
 
 
-def tokens_covering_tile_columns(ids, E, n_extra, seed, tile=192):
+def tokens_covering_tile_columns(ids, E, n_extra, seed, tile=160):
     """Token indices whose assignments together sit at every tile column
     that occurs (greedy), plus n_extra more drawn at random."""
     cols = tile_columns(ids, E, tile)

@@ -75,8 +75,8 @@ SMALL_CASES = [
     S.Workload("pf_k8_e128", 40, 512, 256, 128, 8, 32, S.BF16, S.BF16, True, -5),
     S.Workload("pf_e256_k8", 33, 256, 128, 256, 8, 32, S.F16, S.BF16, False, -6),
     S.Workload("pf_k1", 130, 256, 128, 4, 1, 32, S.F16, S.F16, True, -5),
-    # token tiles wider than 128 columns (up to 192): ~150 tokens per expert
-    # (one tile of 160), and ~500 (three tiles of 167)
+    # token tiles wider than 128 columns (up to 160): ~150 tokens per expert
+    # (one tile of 160), and ~500 (four tiles of 125)
     S.Workload("pf_wide_tile", 300, 256, 128, 2, 1, 32, S.F16, S.F16, True, -5),
     S.Workload("pf_three_wide", 500, 512, 256, 2, 2, 64, S.BF16, S.F16, True, -5),
 ]
@@ -108,7 +108,7 @@ def test_larger_e_prefill_full_size_tile_columns(name):
 
 def test_stack_layer_full_size_tile_columns():
     """One layer of the T = 2048 stack shape (bf16 tokens, fp16 scales, zp):
-    the tokens whose assignments sit at every column position of the 192-
+    the tokens whose assignments sit at every column position of the 160-
     token tiles (all positions that occur), plus 256 more at random."""
     check_prefill(S.WORKLOADS["stack"], seed=2, cover=256)
 
