@@ -170,28 +170,11 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem desc] x B[smem desc]^T, bf16/f16 inputs, f32 accumulate.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Same with A read from tensor memory.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// The same issued by one elected lane of a converged warp: every lane runs
-// the MMA loop, so the operands stay warp-uniform.  Measured on GB300 an
-// elected lane issues a tcgen05.mma about every 32 cycles, a lone active
-// lane of a diverged warp about every 65.
+// D[tmem] (+)= A[tmem] x B[smem desc]^T, bf16/f16 inputs, f32 accumulate,
+// issued by one elected lane of a converged warp: every lane runs the MMA
+// loop, so the operands stay warp-uniform.  Measured on GB300 an elected
+// lane issues a tcgen05.mma about every 32 cycles, a lone active lane of a
+// diverged warp about every 65.
 __device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                                  uint32_t accumulate) {
   asm volatile(
@@ -216,12 +199,6 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
       : "memory");
 }
-// Arrive on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
 // 32 lanes x 16 consecutive 32-bit columns (one row per thread of the
 // warp), waited for in the same asm block so no use of the registers can be
 // scheduled before the data has arrived.
@@ -235,17 +212,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// 32 lanes x 32 consecutive 32-bit columns stored from registers.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 // 32 lanes x 16 consecutive 32-bit columns stored from registers.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -380,37 +346,6 @@ __device__ __forceinline__ void softmax_topk(const float (&lg)[ME], int E, int k
   }
 }
 
-// ------------------------------------------------------- grid barrier
-// One thread per CTA, after a CTA barrier over the threads whose global
-// writes must be published.  ctr[0] counts arrivals, ctr[1] is the
-// generation.  The last arrival releases the waiters first (a release store
-// of the next generation: every arrival's writes precede its atomic add,
-// and the adds are ordered before the last one) and only then resets the
-// count for the next launch, off the waiters' critical path; the next
-// launch arrives only after this grid has completed.  Only valid when all
-// nctas CTAs are co-resident (cooperative launch).  Gives up after
-// ~kWaitLimitCycles: sets QMOE_ST_TIMEOUT and returns false.
-__device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t nctas, uint32_t* status, long long limit) {
-  uint32_t gen;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(ctr + 1) : "memory");
-  __threadfence();
-  const uint32_t old = atomicAdd(ctr, 1u);
-  if (old == nctas - 1) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ctr + 1), "r"(gen + 1u) : "memory");
-    atomicExch(ctr, 0u);
-    return true;
-  }
-  const long long t0 = clock64();
-  for (;;) {
-    uint32_t g;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(ctr + 1) : "memory");
-    if (g != gen) return true;
-    if (clock64() - t0 > limit) {
-      set_status(status, QMOE_ST_TIMEOUT);
-      return false;
-    }
-  }
-}
 
 // ---------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
