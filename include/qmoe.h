@@ -110,7 +110,8 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
  *                 equals DECODE_SPLIT's bit for bit; its output differs from
  *                 DECODE_SPLIT's only by the order of fp32 sums in the down
  *                 projection.
- *   AUTO          DECODE for T <= QMOE_DECODE_MAX_TOKENS, else PREFILL. */
+ *   AUTO          DECODE for T <= QMOE_AUTO_DECODE_MAX_TOKENS, else PREFILL
+ *                 (DECODE where PREFILL's shape rules do not hold). */
 typedef enum {
   QMOE_PATH_AUTO = 0,
   QMOE_PATH_DECODE = 1,
@@ -129,8 +130,15 @@ typedef struct {
 /* Largest shapes accepted: E <= 256 experts, 1 <= k <= 8. */
 #define QMOE_MAX_EXPERTS 256
 #define QMOE_MAX_TOPK 8
-/* Tokens at or below this count take the decode (GEMV) path under QMOE_PATH_AUTO. */
+/* Most tokens the decode (GEMV) path takes (QMOE_PATH_DECODE). */
 #define QMOE_DECODE_MAX_TOKENS 16
+/* Tokens at or below this count take the decode path under QMOE_PATH_AUTO,
+ * more take the grouped GEMM (when its shape rules hold, else decode up to
+ * QMOE_DECODE_MAX_TOKENS).  Measured on GB300 at the Qwen1.5-MoE-A2.7B layer
+ * shape (H 2048, I 1408, E 60, k 4, block 32, fp16, zero points), per layer:
+ * decode 80 / 132 / 182 / 234 us and grouped GEMM 88 / 122 / 150 / 172 us at
+ * T = 4 / 8 / 12 / 16. */
+#define QMOE_AUTO_DECODE_MAX_TOKENS 5
 
 /* Human-readable name of a status code.  Never NULL. */
 const char* qmoe_status_string(int status);
@@ -229,7 +237,7 @@ int qmoe_forward(const void* x, int act_dtype, const void* router_w, const float
                  void* stream);
 
 /* qmoe_forward with an explicit path (QMOE_PATH_*); AUTO picks decode for
- * T <= QMOE_DECODE_MAX_TOKENS. */
+ * T <= QMOE_AUTO_DECODE_MAX_TOKENS. */
 int qmoe_forward_ex(const void* x, int act_dtype, const void* router_w, const float* router_bias,
                     qmoe_qweight gate, qmoe_qweight up, qmoe_qweight down, int scale_dtype, int T,
                     int H, int I, int E, int k, int block_size, void* out, float* topk_w_out,

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libqmoe.so")
 F16, BF16 = 0, 1
 PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_DECODE_SPLIT, PATH_DECODE_FUSED = 0, 1, 2, 4, 5
 DECODE_MAX_TOKENS = 16
+AUTO_DECODE_MAX_TOKENS = 5
 DIAG_STALL_GEMM = 1
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported device or shape",
            3: "workspace missing or too small", 4: "CUDA runtime error",

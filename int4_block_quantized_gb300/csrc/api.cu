@@ -280,7 +280,8 @@ int forward_impl(const void* x, int act_dtype, const void* router_w, const float
   const bool split_decode = path == QMOE_PATH_DECODE_SPLIT;
   const bool force_fused = path == QMOE_PATH_DECODE_FUSED;
   if (split_decode || force_fused) path = QMOE_PATH_DECODE;
-  if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
+  if (path == QMOE_PATH_AUTO)
+    path = dec_ok && (T <= QMOE_AUTO_DECODE_MAX_TOKENS || !pre_ok) ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
   if (path == QMOE_PATH_DECODE && !dec_ok) return QMOE_ERR_UNSUPPORTED;
   if (path == QMOE_PATH_PREFILL && !pre_ok) return QMOE_ERR_UNSUPPORTED;
 
@@ -427,7 +428,8 @@ int qmoe_forward_kernels(int T, int H, int I, int E, int k, int block_size, int 
   const bool dec_ok = T <= kDecodeMaxTokens && decode_fits(kModeGateUp, T, I, H, block_size, zgu, k) &&
                       decode_fits(kModeDown, T, H, I, block_size, zd, k);
   const bool pre_ok = prefill_fits(H, I, block_size, act_dtype, scale_dtype, zgu, zd);
-  if (path == QMOE_PATH_AUTO) path = dec_ok ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
+  if (path == QMOE_PATH_AUTO)
+    path = dec_ok && (T <= QMOE_AUTO_DECODE_MAX_TOKENS || !pre_ok) ? QMOE_PATH_DECODE : QMOE_PATH_PREFILL;
   if (path == QMOE_PATH_DECODE || path == QMOE_PATH_DECODE_SPLIT || path == QMOE_PATH_DECODE_FUSED) {
     if (!dec_ok) return -QMOE_ERR_UNSUPPORTED;
     const bool fits = fused_fits(T, H, I, E, k, block_size, act_dtype, scale_dtype, zgu, zd);

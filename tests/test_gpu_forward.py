@@ -70,12 +70,28 @@ DECODE_CASES = [
 
 @pytest.mark.parametrize("wl", DECODE_CASES, ids=[w.name for w in DECODE_CASES])
 def test_forward_decode_matches_oracle(wl):
-    run_and_check(wl, seed=1)
+    run_and_check(wl, seed=1, path=B.PATH_DECODE)
+
+
+@pytest.mark.parametrize("T,expect", [(1, B.PATH_DECODE), (5, B.PATH_DECODE), (6, B.PATH_PREFILL),
+                                      (16, B.PATH_PREFILL)])
+def test_auto_path_choice(T, expect):
+    """AUTO takes the decode path up to AUTO_DECODE_MAX_TOKENS tokens and the
+    grouped GEMM beyond: AUTO and the forced path both match the oracle, and
+    the kernel count says which path AUTO runs."""
+    base = S.WORKLOADS["verify"]
+    wl = S.Workload("auto%d" % T, T, base.H, base.I, base.E, base.k, base.block_size, base.act_dtype,
+                    base.scale_dtype, base.has_zp, base.scale_exp)
+    L = S.make_layer(wl, seed=11, device=DEV)
+    auto, _ = run_and_check(wl, layer=L, path=B.PATH_AUTO)
+    forced, _ = run_and_check(wl, layer=L, path=expect)
+    n = B.qmoe_forward_kernels(L, T)
+    assert n == (5 if expect == B.PATH_PREFILL else (1 if T == 1 else 3))
 
 
 def test_forward_decode_residual_accumulate():
-    run_and_check(S.WORKLOADS["tiny"], seed=2, accumulate=True)
-    run_and_check(S.WORKLOADS["verify"], seed=2, accumulate=True)
+    run_and_check(S.WORKLOADS["tiny"], seed=2, accumulate=True, path=B.PATH_DECODE)
+    run_and_check(S.WORKLOADS["verify"], seed=2, accumulate=True, path=B.PATH_DECODE)
 
 
 def test_forward_all_tokens_one_expert():
@@ -86,7 +102,8 @@ def test_forward_all_tokens_one_expert():
     bias = torch.zeros(wl.E, device=DEV)
     bias[17] = 30.0
     L["router_bias"] = bias
-    run_and_check(wl, layer=L)
+    run_and_check(wl, layer=L, path=B.PATH_DECODE)
+    run_and_check(wl, layer=L, path=B.PATH_PREFILL)
 
 
 def test_forward_identical_experts_closed_form():
@@ -111,9 +128,9 @@ def test_forward_repeat_calls_identical():
     wl = S.WORKLOADS["verify"]
     L = S.make_layer(wl, seed=6, device=DEV)
     ws = B.Workspace(wl.T, wl.H, wl.I, wl.E, wl.k)
-    a = B.qmoe_forward(L, ws=ws).clone()
+    a = B.qmoe_forward(L, ws=ws, path=B.PATH_DECODE).clone()
     for _ in range(3):
-        assert torch.equal(B.qmoe_forward(L, ws=ws), a)
+        assert torch.equal(B.qmoe_forward(L, ws=ws, path=B.PATH_DECODE), a)
 
 
 def test_forward_decode_full_size_workspace_reuse_across_shapes():

@@ -145,7 +145,9 @@ def test_kernel_count_query():
         with pytest.raises(B.QMoEError, match="unsupported"):
             B.qmoe_forward_kernels(L, T, path=B.PATH_DECODE_FUSED)
     assert B.qmoe_forward_kernels(L, 1, path=B.PATH_DECODE_SPLIT) == 3
-    assert B.qmoe_forward_kernels(L, 16) == 3
+    assert B.qmoe_forward_kernels(L, 5) == 3
+    assert B.qmoe_forward_kernels(L, 16) == 5  # AUTO: the grouped GEMM beyond 5 tokens
+    assert B.qmoe_forward_kernels(L, 16, path=B.PATH_DECODE) == 3
     assert B.qmoe_forward_kernels(L, 512) == 5
     Lt = S.make_layer(S.WORKLOADS["tiny"], seed=10, device=DEV)
     assert B.qmoe_forward_kernels(Lt, 4, path=B.PATH_DECODE_FUSED) == 1
