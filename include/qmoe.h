@@ -80,9 +80,11 @@ typedef enum { QMOE_F16 = 0, QMOE_BF16 = 1 } qmoe_dtype;
  *                 layer runs as one kernel; otherwise as three kernels
  *                 (router; gate-up + SwiGLU; down + weighted sum).  The one
  *                 kernel splits the down projection along I over clusters of
- *                 4 CTAs and sums the partial outputs in a fixed order; it
- *                 has no grid-wide wait, so it runs with any number of SMs
- *                 available, and its results are bit-reproducible.
+ *                 4 CTAs and adds the partial outputs into an integer
+ *                 fixed-point accumulator (2^-32), so the sum does not depend
+ *                 on arrival order; it has no grid-wide wait, so it runs
+ *                 with any number of SMs available, and its results are
+ *                 bit-reproducible.
  *   PREFILL       tokens grouped by expert, grouped GEMM on the tensor cores
  *                 with fp32 accumulation and exact operands: with bf16 block
  *                 scales the operands are fp16 (bf16 activations convert
