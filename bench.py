@@ -38,7 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel from an ncu capture of the current build (profiles/; None: not
 # captured since the kernel last changed)
-NCU_TRAFFIC = {("decode", "layer"): 20924672.0, ("prefill", "gateup"): 132435456.0}
+NCU_TRAFFIC = {("decode", "layer"): 20924672.0, ("prefill", "gateup"): 132435456.0,
+               ("verify", "gateup"): 133735424.0}
 POOL = {"tiny": 4, "decode": 24, "verify": 24, "prefill": 8, "stack": 24,
         "e128_decode": 24, "e128_prefill": 8, "e256_decode": 24, "e256_prefill": 8}
 DEFAULT_STEPS = {"tiny": 2400, "decode": 24000, "verify": 4800, "prefill": 480, "stack": 60,
