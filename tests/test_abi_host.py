@@ -202,3 +202,16 @@ def test_kernel_count_query_rejects_bad_arguments(L):
     assert L.qmoe_forward_kernels(1, 2048, 1408, 300, 4, 32, 0, 0, 1, 1, 0) == -1   # E > 256
     assert L.qmoe_forward_kernels(1, 2048, 1408, 60, 4, 48, 0, 0, 1, 1, 0) == -1    # block size
     assert L.qmoe_forward_kernels(1, 2048, 1408, 60, 4, 32, 0, 0, 1, 1, 6) == -1    # path
+
+
+def test_diagnostics_reject_bad_arguments(L):
+    """qmoe_workspace_set_diagnostics: workspace and flag checks happen on the
+    host before anything is enqueued."""
+    import ctypes
+    f = L.qmoe_workspace_set_diagnostics
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_void_p]
+    assert f(None, 1 << 30, 0, 0, None) == 3          # no workspace
+    assert f(FAKE + 16, 1 << 30, 0, 0, None) == 3     # not 256-byte aligned
+    assert f(FAKE, 64, 0, 0, None) == 3               # smaller than the control block
+    assert f(FAKE, 1 << 30, 0, 2, None) == 1          # unknown flag
