@@ -183,7 +183,10 @@ int qmoe_workspace_set_diagnostics(void* workspace, size_t workspace_bytes, uint
                                    uint32_t flags, void* stream);
 
 /* Router: logits = x[T,H] . router_w[H,E] (+ router_bias[E]) accumulated in
- * fp32; softmax over all E in fp32; the k largest probabilities, best first,
+ * fp32 (on CUDA cores for T <= 16; on the tensor cores for T > 16 when H is
+ * a multiple of 64, E <= 128 and x is 16-byte aligned: exact 16-bit products
+ * summed in fp32, the sum of the K-split partials in a fixed order);
+ * softmax over all E in fp32; the k largest probabilities, best first,
  * equal probabilities ordered by lower expert id; weights are the raw
  * probabilities (not renormalised).  Then the assignments a = t*k + j are
  * grouped by expert ("sort tokens by expert", IR guide Optimization
